@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of one MLA decode step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one pass of the hot path over one batch: query absorption
+(mla_absorb_q), split-KV absorbed attention + combine (mla_decode) and the
+value up-projection (mla_project_out); for the full-layer workload also the
+query projection and the cache append, and W_O.  Inputs are synthetic and
+seeded (workloads.py).  Prints one JSON line (rank 0).
+
+ours:       device-resident inputs; R replicas of every input tensor are
+            rotated so consecutive steps never find their cache, queries or
+            weights in L2 (R * bytes > 2 * L2).  CUDA events on the launching
+            stream; max over ranks.  e2e: the same step preceded by pinned
+            host -> device copies of the step's inputs and followed by a
+            device -> host read of its output.
+reference:  the fp64 CPU oracle (unmerged MLA) on a bounded sample of the
+            same workload, on the host cores.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from head_latent_attention_23_b300 import workloads as W  # noqa: E402
+
+METRIC = "MLA decode tokens/s; latent-cache HBM GB/s & TFLOP/s as % of roofline"
+UNIT = "tokens/s"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="v2_b16_ctx4k", choices=sorted(W.WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--seed", type=int, default=0)
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], tc=d["bf16_tflops"], tc_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6400.0, tc=1800.0, tc_sus=1400.0, src="fallback")
+
+
+def work_per_step(w):
+    """Algorithmic cache bytes and flops of one mla_decode call.
+
+    Per (query, cached token): the cache row (d_latent + d_rope elements) is
+    read once, and each head does a (d_latent + d_rope) dot product for the
+    score and a d_latent axpy for the latent-space value sum.
+    """
+    c = w["cfg"]
+    esz = 2 if c["dtype"] == "bf16" else 4
+    tokens = int(w["seq_lens"].sum())
+    D = c["d_latent"] + c["d_rope"]
+    bytes_ = tokens * D * esz
+    flops = tokens * c["heads"] * (2 * D + 2 * c["d_latent"])
+    return tokens, bytes_, flops
+
+
+def profile_record(kernel_tag):
+    """Per-launch DRAM traffic of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_tag)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "head_latent_attention_23_b300", "csrc", rec["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec if h == rec["source_sha"] else None
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while running."""
+
+    def __init__(self, index):
+        self.samples = []
+        self.reasons = set()
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.max_mhz = None
+        self._stop = threading.Event()
+
+    def _run(self):
+        nv = self.nv
+        names = {
+            "hw_slowdown": getattr(nv, "nvmlClocksEventReasonHwSlowdown", 0x8),
+            "hw_thermal_slowdown": getattr(nv, "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
+            "sw_thermal_slowdown": getattr(nv, "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
+            "sw_power_cap": getattr(nv, "nvmlClocksEventReasonSwPowerCap", 0x4),
+            "hw_power_brake_slowdown": getattr(nv, "nvmlClocksEventReasonHwPowerBrakeSlowdown",
+                                               0x80),
+        }
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                try:
+                    r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                except AttributeError:
+                    r = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
+                for k, bit in names.items():
+                    if r & bit:
+                        self.reasons.add(k)
+            except Exception:
+                pass
+            time.sleep(0.02)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def cpu_sample(w, seconds_target=12.0, max_rounds=64):
+    """Times the oracle (as it stands) on whole sequences' worth of heads.
+
+    One 'round' decodes `threads` (sequence, head) pairs, one per oracle
+    thread, over sequence 0's full context; rounds repeat until about
+    `seconds_target` of wall time.  Returns (tokens/s, threads, description).
+    """
+    import oracle as O
+    v = W.oracle_view(w)
+    H = w["cfg"]["heads"]
+    threads = O.num_threads()
+    done_heads = 0
+    t0 = time.perf_counter()
+    rounds = 0
+    while True:
+        pairs = [(0, (done_heads + k) % H) for k in range(threads)]
+        if w["kind"] == "cached":
+            O.reference_cached_decode(v, pairs=pairs)
+        else:
+            O.reference_token_decode(v, seqs=[0], pairs=[(0, h) for _, h in pairs])
+        done_heads += threads
+        rounds += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target or rounds >= max_rounds:
+            break
+    tokens = done_heads / H          # one decode token = all heads of one sequence
+    n0 = int(w["seq_lens"][0])
+    desc = (f"{done_heads} (sequence, head) pairs of sequence 0 (context {n0}) of "
+            f"{w_name(w)}; {tokens:.3f} decode tokens in {el:.2f} s")
+    return tokens / el, threads, desc
+
+
+def w_name(w):
+    return w.get("_name", "workload")
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle as O
+    w = W.WORKLOADS[args.workload](args.seed)
+    w["_name"] = args.workload
+    v = W.oracle_view(w)
+    H = w["cfg"]["heads"]
+    threads = O.num_threads()
+    K = args.steps if args.steps else 5
+
+    def step(i):
+        pairs = [(0, (i * threads + k) % H) for k in range(threads)]
+        if w["kind"] == "cached":
+            O.reference_cached_decode(v, pairs=pairs)
+        else:
+            O.reference_token_decode(v, seqs=[0], pairs=[(0, h) for _, h in pairs])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    tokens = K * threads / H
+    val = tokens / el
+    cfg = config_block(w, args.workload, 1, "n/a (host)")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws,
+        "steps": K, "warmup": args.warmup, "ms_per_step": el / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; shapes of the pages' DeepSeek-V2 figures)", "config": cfg,
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {threads} (sequence 0, head) pairs "
+                                   f"= {threads}/{H} of one decode token"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def config_block(w, name, replicas, l2):
+    c = w["cfg"]
+    lens = w["seq_lens"]
+    return {"workload": name, "batch": int(w["batch"]), "heads": c["heads"],
+            "d_latent": c["d_latent"], "d_rope": c["d_rope"], "d_nope": c["d_nope"],
+            "d_v": c["d_v"], "block_size": c["block_size"],
+            "context_min": int(lens.min()), "context_max": int(lens.max()),
+            "context_total": int(lens.sum()), "parallelism": "replicas",
+            "l2": l2, "input_replicas": replicas}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    from head_latent_attention_23_b300 import mla
+    from head_latent_attention_23_b300.runner import DecodeStep
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload](args.seed + rank)
+    w["_name"] = args.workload
+    tokens, cbytes, cflops = work_per_step(w)
+    step_bytes = sum(t.numel() * t.element_size() for t in w.values()
+                     if isinstance(t, torch.Tensor))
+    R = max(1, math.ceil(2 * L2_BYTES / max(step_bytes, 1)) + 1)
+    R = min(R, 8)
+    steps = [DecodeStep(w, dev) for _ in range(R)]
+    stream = torch.cuda.current_stream(dev)
+    B = w["batch"]
+
+    for i in range(max(args.warmup, 3)):
+        steps[i % R].run()
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK, "device status after warm-up"
+
+    K = args.steps
+    if K is None:
+        t0 = time.perf_counter()
+        for i in range(10):
+            steps[i % R].run()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 10
+        K = int(min(max(2.0 / per, 50), 20000))
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(K):
+            _run_with_decode_events(steps[i % R], ev[i], stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert mla.get_status() == mla.MLA_OK, "device status after timed region"
+
+    # end to end: pinned host inputs -> device, step, result -> host
+    e2e = run_e2e(steps[0], w, dev, stream, max(20, min(K, 2000)))
+
+    if rank != 0:
+        return
+    pk = peaks()
+    ms_step = total_ms / K
+    value = ws * B * K / (total_ms / 1e3)
+    dec_mean_ms = statistics.mean(dec_ms)
+    dec_med_ms = statistics.median(dec_ms)
+    hbm_gbs = cbytes / (dec_mean_ms * 1e-3) / 1e9
+    tflops = cflops / (dec_mean_ms * 1e-3) / 1e12
+    t_roof = max(cbytes / (pk["hbm"] * 1e9), cflops / (pk["tc"] * 1e12))
+    bound = "hbm" if cbytes / (pk["hbm"] * 1e9) >= cflops / (pk["tc"] * 1e12) else "tensor"
+    path = mla.decode_path(steps[0].cfg)
+    rec = profile_record("decode_tc" if path == 1 else "decode_simt")
+    roof = {
+        "bound": bound,
+        "achieved": hbm_gbs if bound == "hbm" else tflops,
+        "peak": pk["hbm"] if bound == "hbm" else pk["tc"],
+        "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+        "frac": (hbm_gbs / pk["hbm"]) if bound == "hbm" else (tflops / pk["tc"]),
+        "traffic": rec["dram_bytes_per_launch"] if rec else None,
+        "kernel": "mla_decode (split-KV core + combine), one call per step",
+        "algorithmic_bytes_per_launch": cbytes,
+        "algorithmic_flops_per_launch": cflops,
+        "tensor_tflops": tflops,
+        "tensor_frac_burst": tflops / pk["tc"],
+        "tensor_frac_sustained": tflops / pk["tc_sus"],
+        "roofline_frac": t_roof / (dec_mean_ms * 1e-3),
+        "decode_ms_mean": dec_mean_ms, "decode_ms_median": dec_med_ms,
+        "peak_source": pk["src"] + " (MEASURED_PEAKS.json burst figures)",
+        "decode_path": "tcgen05" if path == 1 else "cuda-core fp32",
+    }
+    try:
+        cpu_val, cores, desc = cpu_sample(w)
+        cpu = {"value": cpu_val, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": desc}
+    except Exception as e:  # the oracle is a baseline only; report why it is missing
+        cpu = {"value": None, "unit": UNIT, "cores": None, "kind": "oracle",
+               "sample": f"unavailable: {e}"}
+    dt = w["cfg"]["dtype"]
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dt,
+        "data": "synthetic (seeded; shapes of the pages' DeepSeek-V2 figures)",
+        "config": config_block(w, args.workload, R,
+                               f"inputs rotated over {R} replicas "
+                               f"({R * step_bytes / 2**20:.0f} MiB > 2 x L2)"),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * steps[0].kernels_per_step(),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def _run_with_decode_events(s, evpair, stream):
+    """One step with CUDA events around its mla_decode call."""
+    from head_latent_attention_23_b300 import mla
+    if s.kind == "token":
+        mla.query_proj(s.cfg, s.x_q, s.w_uq, s.pos_q, s.q_nope, s.q_pe, w_dq=s.w_dq,
+                       scratch=s.q_scratch)
+        mla.append_latent(s.cfg, s.x_new, s.w_dkv, s.seq_idx_new, s.pos_new, s.block_table,
+                          s.cache)
+    mla.absorb_q(s.cfg, s.q_nope, s.w_uk, s.q_lat)
+    evpair[0].record(stream)
+    s.decode()
+    evpair[1].record(stream)
+    if s.kind == "token":
+        mla.project_out(s.cfg, s.o_lat, s.w_uv, s.o_v, s.w_o, s.out)
+    else:
+        mla.project_out(s.cfg, s.o_lat, s.w_uv, s.o_v)
+
+
+def run_e2e(s, w, dev, stream, K):
+    """Same step through the public calls, with the step's inputs copied from
+    pinned host memory and its output read back every step."""
+    if s.kind == "cached":
+        ins = [("q_nope", s.q_nope), ("q_pe", s.q_pe), ("seq_lens", s.seq_lens),
+               ("block_table", s.block_table)]
+        result = s.o_v
+    else:
+        ins = [("x_q", s.x_q), ("pos_q", s.pos_q), ("x_new", s.x_new),
+               ("seq_lens", s.seq_lens), ("block_table", s.block_table)]
+        result = s.out
+    host_in = [(d, d.cpu().pin_memory()) for _, d in ins]
+    host_out = torch.empty(result.shape, dtype=result.dtype).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    for _ in range(3):
+        for d, h in host_in:
+            d.copy_(h, non_blocking=True)
+        s.run()
+        host_out.copy_(result, non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        for d, h in host_in:
+            d.copy_(h, non_blocking=True)
+        s.run()
+        host_out.copy_(result, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    return {"value": w["batch"] / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K,
+            "note": "same input set every step (L2-warm weights and cache)"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,113 @@
+// Internal helpers shared by the libmla.so translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "mla.h"
+
+namespace mla {
+
+// ---------------------------------------------------------------- elements
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// First error wins; later ones are dropped.
+__device__ __forceinline__ void flag(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- split plan
+// The decode work is the sequence of 64-token tiles of all sequences laid end
+// to end.  Worker g of W takes the tile range [lo(g), lo(g+1)), which can
+// cross sequence boundaries; each (worker, sequence) piece yields one partial
+// result in slot g + b.  Slots are unique (ranges are ordered) and fewer than
+// W + batch.
+constexpr int kTile = 64;
+
+__host__ __device__ __forceinline__ int64_t plan_lo(int g, int64_t total, int W) {
+    return (int64_t)g * total / W;
+}
+
+// Seq length actually used: out-of-range lengths are flagged and clamped.
+__device__ __forceinline__ int clamp_len(int n, int cap, int* status) {
+    if (n < 1 || n > cap) {
+        flag(status, MLA_ERR_INVALID_ARG);
+        return n < 1 ? 0 : cap;
+    }
+    return n;
+}
+
+// Block-wide exclusive prefix of ceil(len_b / kTile) over b = 0..batch-1 into
+// pre[0..batch] (shared).  All threads must call.
+__device__ __forceinline__ void tile_prefix(const int32_t* seq_lens, int batch, int cap,
+                                            int* pre, int* status) {
+    __shared__ int warp_tot[32];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    int carry = 0;
+    for (int base = 0; base < batch; base += nt) {
+        int b = base + tid;
+        int v = 0;
+        if (b < batch) v = (clamp_len(seq_lens[b], cap, status) + kTile - 1) / kTile;
+        // inclusive scan within the warp
+        int lane = tid & 31, w = tid >> 5;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[w] = x;
+        __syncthreads();
+        int off = 0;
+        for (int k = 0; k < w; ++k) off += warp_tot[k];
+        if (b < batch) pre[b] = carry + off + x - v;
+        int chunk = 0;
+        for (int k = 0; k < (nt + 31) / 32; ++k) chunk += warp_tot[k];
+        __syncthreads();
+        carry += chunk;
+    }
+    if (tid == 0) pre[batch] = carry;
+    __syncthreads();
+}
+
+// Index of the sequence holding global tile t: largest b with pre[b] <= t.
+__device__ __forceinline__ int seq_of_tile(const int* pre, int batch, int64_t t) {
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+}  // namespace mla

@@ -1,0 +1,80 @@
+// Internal launch interface between the C-ABI layer (mla_api.cu) and the
+// kernel translation units.  Host code only; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mla {
+
+struct DecodeArgs {
+    int heads, d_latent, d_rope, block_size, max_blocks, batch;
+    int workers;            // W: tile ranges the context is split into
+    int64_t num_blocks;
+    float scale;
+    const void* q_lat;      // [batch][heads][d_latent]
+    const void* q_pe;       // [batch][heads][d_rope]
+    const void* cache;      // [num_blocks][block_size][d_latent + d_rope]
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    float* o_part;          // [W + batch][heads][d_latent]
+    float* lse_part;        // [W + batch][heads]
+    void* o_lat;            // [batch][heads][d_latent]
+    float* lse;             // [batch][heads] or null
+    int* status;
+};
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t st);
+size_t decode_simt_smem(const DecodeArgs& a);
+
+// Tensor-core decode (bf16, 128 heads, d_latent 512, d_rope 64, pages of a
+// multiple of 64 tokens).  Returns cudaErrorNotSupported when the device or
+// the shapes do not fit it.
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
+int decode_tc_workers(int num_sms);
+bool decode_tc_supported(int heads, int d_latent, int d_rope, int block_size, int dtype);
+
+// Merge of the partials written by a decode kernel (slots g + b of plan W).
+cudaError_t launch_combine_planned(const DecodeArgs& a, int dtype, cudaStream_t st);
+// Merge of dense partials [n_splits][batch][heads][d_latent].
+cudaError_t launch_combine_dense(const float* o_part, const float* lse_part, int n_splits,
+                                 int batch, int heads, int d_latent, void* o_lat, float* lse,
+                                 int dtype, cudaStream_t st);
+
+struct AppendArgs {
+    int n_tok, d_in, d_latent, d_rope, block_size, max_blocks, batch;
+    int64_t num_blocks;
+    double rope_base;
+    const void* x;          // [n_tok][d_in]
+    const void* w_dkv;      // [d_in][d_latent + d_rope]
+    const int32_t* seq_idx;
+    const int32_t* pos;
+    const int32_t* block_table;
+    void* cache;
+    void* dense_out;        // or null
+    float* rows_f32;        // optional precomputed fp32 rows [n_tok][d_latent + d_rope]
+    int* status;
+};
+cudaError_t launch_append(const AppendArgs& a, int dtype, cudaStream_t st);
+
+// Batched strided GEMM on CUDA cores, fp32 accumulation:
+//   C[z][m][n] = sum_k A[z][m][k] * B[z][k][n]
+// element (m,k) of A at A + z*sA + m*sAm + k*sAk (likewise B, C).
+struct GemmArgs {
+    int M, N, K, batch;
+    const void* A; int64_t sA, sAm, sAk;
+    const void* B; int64_t sB, sBk, sBn;
+    void* C; int64_t sC, sCm, sCn;
+};
+// Element types of A, B and C: MLA_DTYPE_*.
+cudaError_t launch_gemm_simt(const GemmArgs& g, int a_dtype, int b_dtype, int c_dtype,
+                             cudaStream_t st);
+
+// Splits fp32 per-head query rows [batch][heads][d_nope + d_rope] into
+// q_nope and the rotated q_pe (dtype).
+cudaError_t launch_q_split_rope(const float* q_all, int batch, int heads, int d_nope,
+                                int d_rope, const int32_t* pos, double rope_base, void* q_nope,
+                                void* q_pe, int dtype, cudaStream_t st);
+
+}  // namespace mla

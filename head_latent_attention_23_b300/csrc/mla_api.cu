@@ -1,0 +1,290 @@
+// C ABI of libmla.so: argument validation, workspace carving and kernel
+// launches.  Every entry point is declared, with its contract, in mla.h.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace mla;
+
+namespace {
+
+// Device-side error word (first error wins).  Its device address is looked
+// up once per device and handed to the kernels as a plain pointer.
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+int current_device(int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices)
+        return MLA_ERR_CUDA;
+    return MLA_OK;
+}
+
+int status_ptr(int** out) {
+    int dev;
+    if (int rc = current_device(&dev)) return rc;
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MLA_ERR_CUDA;
+        g_status_ptr[dev] = (int*)p;
+    }
+    *out = g_status_ptr[dev];
+    return MLA_OK;
+}
+
+int num_sms(int* out) {
+    int dev;
+    if (int rc = current_device(&dev)) return rc;
+    if (!g_num_sms[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MLA_ERR_CUDA;
+        g_num_sms[dev] = v;
+    }
+    *out = g_num_sms[dev];
+    return MLA_OK;
+}
+
+int check_cfg(const mla_config* c) {
+    if (!c) return MLA_ERR_INVALID_ARG;
+    if (c->heads < 1 || c->heads > 1024) return MLA_ERR_INVALID_ARG;
+    if (c->d_latent < 1 || c->d_latent > 4096) return MLA_ERR_INVALID_ARG;
+    if (c->d_rope < 0 || c->d_rope > 1024 || (c->d_rope & 1)) return MLA_ERR_INVALID_ARG;
+    if (c->d_nope < 1 || c->d_nope > 4096 || c->d_v < 1 || c->d_v > 4096)
+        return MLA_ERR_INVALID_ARG;
+    if (c->block_size < 1 || c->block_size > (1 << 20)) return MLA_ERR_INVALID_ARG;
+    if (c->dtype != MLA_DTYPE_BF16 && c->dtype != MLA_DTYPE_F32) return MLA_ERR_INVALID_ARG;
+    if (!isfinite(c->softmax_scale) || !isfinite(c->rope_base) || c->rope_base <= 0.0)
+        return MLA_ERR_INVALID_ARG;
+    return MLA_OK;
+}
+
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+constexpr int kMaxDecodeBatch = 8192;
+
+bool use_tc(const mla_config* c) {
+    return decode_tc_supported(c->heads, c->d_latent, c->d_rope, c->block_size, c->dtype);
+}
+
+// Split-KV worker count of the decode kernel that `c` selects.
+int decode_workers(const mla_config* c, int* W) {
+    int sms;
+    if (int rc = num_sms(&sms)) return rc;
+    *W = use_tc(c) ? decode_tc_workers(sms) : sms;
+    return MLA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t decode_ws_bytes(const mla_config* c, int W, int batch) {
+    size_t slots = (size_t)W + (size_t)batch;
+    return align256(slots * c->heads * c->d_latent * sizeof(float)) +
+           align256(slots * c->heads * sizeof(float));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int s) {
+    switch (s) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case MLA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MLA_ERR_CUDA: return "CUDA error";
+        case MLA_ERR_TIMEOUT: return "device wait timed out";
+        case MLA_ERR_INDEX: return "block id or sequence index out of range";
+        default: return "unknown status";
+    }
+}
+
+int mla_version(void) { return 100; }
+
+int mla_get_status(mla_stream_t stream, int* out) {
+    if (!out) return MLA_ERR_INVALID_ARG;
+    int* p;
+    if (int rc = status_ptr(&p)) return rc;
+    int v = 0, zero = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaMemcpyAsync(p, &zero, sizeof(int), cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+    *out = v;
+    return MLA_OK;
+}
+
+int mla_decode_path(const mla_config* cfg) {
+    if (check_cfg(cfg)) return -1;
+    return use_tc(cfg) ? 1 : 0;
+}
+
+int mla_append_latent(const mla_config* cfg, const void* x, int n_tok, int d_in,
+                      const void* w_dkv, const int32_t* seq_idx, const int32_t* pos,
+                      const int32_t* block_table, int batch, int max_blocks, void* cache,
+                      int64_t num_blocks, void* dense_out, mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (n_tok < 0 || d_in < 1 || d_in > 65536 || batch < 1 || max_blocks < 1 ||
+        num_blocks < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (n_tok == 0) return MLA_OK;
+    if (!x || !w_dkv || !seq_idx || !pos || !block_table || !cache) return MLA_ERR_INVALID_ARG;
+    if ((size_t)(d_in + cfg->d_latent + cfg->d_rope) * sizeof(float) > 200 * 1024)
+        return MLA_ERR_UNSUPPORTED;
+    int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    AppendArgs a{};
+    a.n_tok = n_tok; a.d_in = d_in; a.d_latent = cfg->d_latent; a.d_rope = cfg->d_rope;
+    a.block_size = cfg->block_size; a.max_blocks = max_blocks; a.batch = batch;
+    a.num_blocks = num_blocks; a.rope_base = cfg->rope_base; a.x = x; a.w_dkv = w_dkv;
+    a.seq_idx = seq_idx; a.pos = pos; a.block_table = block_table; a.cache = cache;
+    a.dense_out = dense_out; a.rows_f32 = nullptr; a.status = status;
+    return cuda_rc(launch_append(a, cfg->dtype, (cudaStream_t)stream));
+}
+
+int mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* w_uk, int batch,
+                 void* q_lat, mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (batch < 0) return MLA_ERR_INVALID_ARG;
+    if (batch == 0) return MLA_OK;
+    if (!q_nope || !w_uk || !q_lat) return MLA_ERR_INVALID_ARG;
+    const int H = cfg->heads, DL = cfg->d_latent, DN = cfg->d_nope;
+    // per head h: q_lat[:, h, :] (batch x DL) = q_nope[:, h, :] (batch x DN) . W_LK_h^T
+    GemmArgs g{};
+    g.M = batch; g.N = DL; g.K = DN; g.batch = H;
+    g.A = q_nope; g.sA = DN; g.sAm = (int64_t)H * DN; g.sAk = 1;
+    g.B = w_uk; g.sB = (int64_t)DL * DN; g.sBk = 1; g.sBn = DN;
+    g.C = q_lat; g.sC = DL; g.sCm = (int64_t)H * DL; g.sCn = 1;
+    return cuda_rc(launch_gemm_simt(g, cfg->dtype, cfg->dtype, cfg->dtype, (cudaStream_t)stream));
+}
+
+int mla_decode_workspace_size(const mla_config* cfg, int batch, size_t* bytes) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (!bytes || batch < 1 || batch > kMaxDecodeBatch) return MLA_ERR_INVALID_ARG;
+    int W;
+    if (int rc = decode_workers(cfg, &W)) return rc;
+    *bytes = decode_ws_bytes(cfg, W, batch);
+    return MLA_OK;
+}
+
+int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const void* cache,
+               int64_t num_blocks, const int32_t* block_table, int max_blocks,
+               const int32_t* seq_lens, int batch, void* o_lat, float* lse, void* workspace,
+               size_t ws_bytes, mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (batch < 1 || batch > kMaxDecodeBatch || max_blocks < 1 || num_blocks < 1)
+        return MLA_ERR_INVALID_ARG;
+    if ((int64_t)max_blocks * cfg->block_size > (int64_t)1 << 30) return MLA_ERR_INVALID_ARG;
+    if (!q_lat || (!q_pe && cfg->d_rope > 0) || !cache || !block_table || !seq_lens || !o_lat)
+        return MLA_ERR_INVALID_ARG;
+    int W;
+    if (int rc = decode_workers(cfg, &W)) return rc;
+    const size_t need = decode_ws_bytes(cfg, W, batch);
+    if (!workspace || ws_bytes < need || ((uintptr_t)workspace & 255)) return MLA_ERR_WORKSPACE;
+    int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    const size_t slots = (size_t)W + batch;
+    DecodeArgs a{};
+    a.heads = cfg->heads; a.d_latent = cfg->d_latent; a.d_rope = cfg->d_rope;
+    a.block_size = cfg->block_size; a.max_blocks = max_blocks; a.batch = batch;
+    a.workers = W; a.num_blocks = num_blocks; a.scale = cfg->softmax_scale;
+    a.q_lat = q_lat; a.q_pe = q_pe; a.cache = cache; a.block_table = block_table;
+    a.seq_lens = seq_lens; a.o_lat = o_lat; a.lse = lse; a.status = status;
+    a.o_part = (float*)workspace;
+    a.lse_part = (float*)((char*)workspace +
+                          align256(slots * cfg->heads * cfg->d_latent * sizeof(float)));
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = use_tc(cfg) ? launch_decode_tc(a, st) : launch_decode_simt(a, cfg->dtype, st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    return cuda_rc(launch_combine_planned(a, cfg->dtype, st));
+}
+
+int mla_decode_combine(const mla_config* cfg, const float* o_part, const float* lse_part,
+                       int n_splits, int batch, void* o_lat, float* lse, mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (n_splits < 1 || n_splits > 1024 || batch < 1) return MLA_ERR_INVALID_ARG;
+    if (!o_part || !lse_part || !o_lat) return MLA_ERR_INVALID_ARG;
+    return cuda_rc(launch_combine_dense(o_part, lse_part, n_splits, batch, cfg->heads,
+                                        cfg->d_latent, o_lat, lse, cfg->dtype,
+                                        (cudaStream_t)stream));
+}
+
+int mla_project_out(const mla_config* cfg, const void* o_lat, const void* w_uv, int batch,
+                    void* o_v, const void* w_o, int d_model, void* out, mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (batch < 0 || (w_o && d_model < 1)) return MLA_ERR_INVALID_ARG;
+    if (batch == 0) return MLA_OK;
+    if (!o_lat || !w_uv || !o_v || (w_o && !out)) return MLA_ERR_INVALID_ARG;
+    const int H = cfg->heads, DL = cfg->d_latent, DV = cfg->d_v;
+    cudaStream_t st = (cudaStream_t)stream;
+    // per head h: o_v[:, h, :] (batch x DV) = o_lat[:, h, :] (batch x DL) . W_LV_h (DL x DV)
+    GemmArgs g{};
+    g.M = batch; g.N = DV; g.K = DL; g.batch = H;
+    g.A = o_lat; g.sA = DL; g.sAm = (int64_t)H * DL; g.sAk = 1;
+    g.B = w_uv; g.sB = (int64_t)DL * DV; g.sBk = DV; g.sBn = 1;
+    g.C = o_v; g.sC = DV; g.sCm = (int64_t)H * DV; g.sCn = 1;
+    if (int rc = cuda_rc(launch_gemm_simt(g, cfg->dtype, cfg->dtype, cfg->dtype, st))) return rc;
+    if (!w_o) return MLA_OK;
+    // out (batch x d_model) = o_v viewed as batch x (H*DV) . W_O
+    GemmArgs o{};
+    o.M = batch; o.N = d_model; o.K = H * DV; o.batch = 1;
+    o.A = o_v; o.sAm = (int64_t)H * DV; o.sAk = 1;
+    o.B = w_o; o.sBk = d_model; o.sBn = 1;
+    o.C = out; o.sCm = d_model; o.sCn = 1;
+    return cuda_rc(launch_gemm_simt(o, cfg->dtype, cfg->dtype, cfg->dtype, st));
+}
+
+int mla_query_proj_workspace_size(const mla_config* cfg, int batch, int d_lq, size_t* bytes) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (!bytes || batch < 1 || d_lq < 0) return MLA_ERR_INVALID_ARG;
+    *bytes = align256((size_t)batch * d_lq * sizeof(float)) +
+             align256((size_t)batch * cfg->heads * (cfg->d_nope + cfg->d_rope) * sizeof(float));
+    return MLA_OK;
+}
+
+int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, const void* w_dq,
+                   int d_lq, const void* w_uq, const int32_t* pos, void* q_nope, void* q_pe,
+                   void* scratch, size_t scratch_bytes, mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (batch < 1 || d_in < 1 || (w_dq && d_lq < 1)) return MLA_ERR_INVALID_ARG;
+    if (!x || !w_uq || !pos || !q_nope || (!q_pe && cfg->d_rope > 0)) return MLA_ERR_INVALID_ARG;
+    const int dlq = w_dq ? d_lq : 0;
+    size_t need;
+    mla_query_proj_workspace_size(cfg, batch, dlq, &need);
+    if (!scratch || scratch_bytes < need || ((uintptr_t)scratch & 255)) return MLA_ERR_WORKSPACE;
+    const int H = cfg->heads, DQ = cfg->d_nope + cfg->d_rope;
+    cudaStream_t st = (cudaStream_t)stream;
+    float* cq = (float*)scratch;
+    float* q_all = (float*)((char*)scratch + align256((size_t)batch * dlq * sizeof(float)));
+    const void* a_in = x;
+    int a_dtype = cfg->dtype, k_in = d_in;
+    if (w_dq) {
+        GemmArgs g{};
+        g.M = batch; g.N = d_lq; g.K = d_in; g.batch = 1;
+        g.A = x; g.sAm = d_in; g.sAk = 1;
+        g.B = w_dq; g.sBk = d_lq; g.sBn = 1;
+        g.C = cq; g.sCm = d_lq; g.sCn = 1;
+        if (int rc = cuda_rc(launch_gemm_simt(g, cfg->dtype, cfg->dtype, MLA_DTYPE_F32, st)))
+            return rc;
+        a_in = cq; a_dtype = MLA_DTYPE_F32; k_in = d_lq;
+    }
+    GemmArgs u{};
+    u.M = batch; u.N = H * DQ; u.K = k_in; u.batch = 1;
+    u.A = a_in; u.sAm = k_in; u.sAk = 1;
+    u.B = w_uq; u.sBk = (int64_t)H * DQ; u.sBn = 1;
+    u.C = q_all; u.sCm = (int64_t)H * DQ; u.sCn = 1;
+    if (int rc = cuda_rc(launch_gemm_simt(u, a_dtype, cfg->dtype, MLA_DTYPE_F32, st))) return rc;
+    return cuda_rc(launch_q_split_rope(q_all, batch, H, cfg->d_nope, cfg->d_rope, pos,
+                                       cfg->rope_base, q_nope, q_pe, cfg->dtype, st));
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+"""One decode step of an MLA layer, as a chain of libmla.so calls.
+
+``DecodeStep`` uploads a workload (see ``workloads``) to the GPU once, owns the
+output and scratch buffers, and ``run()`` issues the step's library calls on
+one stream.  Nothing here computes: it only orders the calls.
+
+Step for a workload whose cache rows are given (shared-cache decode):
+    mla_absorb_q -> mla_decode (split-KV core + combine) -> mla_project_out
+Step for a workload driven by hidden states x (full layer):
+    mla_query_proj -> mla_append_latent -> mla_absorb_q -> mla_decode
+    -> mla_project_out (with W_O)
+"""
+import torch
+
+from . import mla
+
+
+class DecodeStep:
+    def __init__(self, w, device="cuda"):
+        self.w = w
+        self.cfg_dict = w["cfg"]
+        self.cfg = mla.config_from(self.cfg_dict)
+        self.kind = w["kind"]
+        dev = torch.device(device)
+        self.device = dev
+        c = self.cfg_dict
+        B, H = w["batch"], c["heads"]
+        dt = torch.bfloat16 if c["dtype"] == "bf16" else torch.float32
+
+        def up(name):
+            t = w.get(name)
+            return None if t is None else t.to(dev).contiguous()
+
+        self.cache = up("cache")
+        self.block_table = up("block_table")
+        self.seq_lens = up("seq_lens")
+        self.w_uk = up("w_uk")
+        self.w_uv = up("w_uv")
+        self.B = B
+        if self.kind == "cached":
+            self.q_nope = up("q_nope")
+            self.q_pe = up("q_pe")
+        else:
+            self.x_new = up("x_new")
+            self.seq_idx_new = up("seq_idx_new")
+            self.pos_new = up("pos_new")
+            self.x_q = up("x_q")
+            self.pos_q = up("pos_q")
+            self.w_dkv = up("w_dkv")
+            self.w_dq = up("w_dq")
+            self.w_uq = up("w_uq")
+            self.w_o = up("w_o")
+            self.q_nope = torch.empty((B, H, c["d_nope"]), dtype=dt, device=dev)
+            self.q_pe = torch.empty((B, H, c["d_rope"]), dtype=dt, device=dev)
+            d_lq = w["d_lq"] or 0
+            self.q_scratch = torch.empty(mla.query_proj_workspace_size(self.cfg, B, d_lq),
+                                         dtype=torch.uint8, device=dev)
+            self.out = torch.empty((B, w["d_model"]), dtype=dt, device=dev)
+        self.q_lat = torch.empty((B, H, c["d_latent"]), dtype=dt, device=dev)
+        self.o_lat = torch.empty((B, H, c["d_latent"]), dtype=dt, device=dev)
+        self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+        self.o_v = torch.empty((B, H, c["d_v"]), dtype=dt, device=dev)
+        self.workspace = mla.decode_workspace(self.cfg, B, dev)
+
+    # the graded core: split-KV attention + combine
+    def decode(self, stream=None):
+        mla.decode(self.cfg, self.q_lat, self.q_pe, self.cache, self.block_table,
+                   self.seq_lens, self.o_lat, self.lse, self.workspace, stream)
+
+    def run(self, stream=None):
+        if self.kind == "token":
+            mla.query_proj(self.cfg, self.x_q, self.w_uq, self.pos_q, self.q_nope, self.q_pe,
+                           w_dq=self.w_dq, scratch=self.q_scratch, stream=stream)
+            mla.append_latent(self.cfg, self.x_new, self.w_dkv, self.seq_idx_new, self.pos_new,
+                              self.block_table, self.cache, stream=stream)
+        mla.absorb_q(self.cfg, self.q_nope, self.w_uk, self.q_lat, stream)
+        self.decode(stream)
+        if self.kind == "token":
+            mla.project_out(self.cfg, self.o_lat, self.w_uv, self.o_v, self.w_o, self.out,
+                            stream)
+        else:
+            mla.project_out(self.cfg, self.o_lat, self.w_uv, self.o_v, stream=stream)
+
+    def kernels_per_step(self):
+        """Kernel launches one run() issues."""
+        n = 1 + 2 + 1                       # absorb, decode core + combine, o_v
+        if self.kind == "token":
+            n += (2 if self.w_dq is not None else 1) + 1   # query GEMM(s) + split/rope
+            n += 1                          # append
+            n += 1                          # W_O
+        return n
+
+    def results(self):
+        r = dict(o_lat=self.o_lat, lse=self.lse, o_v=self.o_v, q_lat=self.q_lat)
+        if self.kind == "token":
+            r["out"] = self.out
+            r["q_nope"] = self.q_nope
+            r["q_pe"] = self.q_pe
+        return r

@@ -1,0 +1,226 @@
+/*
+ * mla.h -- C ABI of libmla.so, Multi-Head Latent Attention (MLA) decode on
+ * NVIDIA B300 (sm_103a).
+ *
+ * What is computed (row-vector notation of "Multi-Head Latent Attention
+ * (MLA)", section "The construction"):
+ *   every cached token i keeps ONE row [c_i | kr_i] shared by all heads:
+ *     c_i  = x_i W_L               latent, d_latent values
+ *     kr_i = RoPE(x_i W_KR, i)     decoupled rotary key part, d_rope values
+ *   a decode step for the newest token t of a sequence of n tokens computes,
+ *   per head h, attention of its query over the n cached rows
+ *     s_i   = scale * (q_lat_h . c_i + q_pe_h . kr_i),  i = 0..n-1
+ *     p     = softmax(s)
+ *     o_lat_h = sum_i p_i c_i
+ *   where q_lat_h = q_nope_h W_LK_h^T is the query pre-multiplied by the
+ *   head's latent-to-key weights (the first merge of "Two merges are where
+ *   the compute win comes from"), and the head output is o_lat_h W_LV_h,
+ *   stacked over heads and multiplied by W_O (the second merge).  Per-head
+ *   keys and values are never formed.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE memory owned by the caller, row-major,
+ *     of the element type given by mla_config.dtype unless stated otherwise
+ *     (int32 index arrays, float32 log-sum-exp and partial outputs).  The
+ *     library never allocates device memory; scratch space is passed in.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream)
+ *     and returns an mla_status.  Host-side validation failures launch
+ *     nothing.  Faults that only the device can see (a block id outside the
+ *     pool, a sequence length out of range) are recorded in a per-device
+ *     status word; the offending rows are skipped, never read out of bounds.
+ *     Read and clear it with mla_get_status().
+ *   - No C++ exception crosses this boundary.
+ *   - Weights use the [in][out] layout of the row-vector formulas: a vector
+ *     times W_X means  y[j] = sum_k x[k] * W_X[k][j].
+ *   - Paged cache: `cache` is [num_blocks][block_size][d_latent + d_rope].
+ *     Logical token i of sequence b lives in row
+ *       block_table[b * max_blocks + i / block_size] * block_size + i % block_size.
+ *     ("MLA: how DeepSeek cuts KV cache memory", section "Where MLA sits in
+ *     the taxonomy": paged cache management.)
+ *   - Positions: key i of a sequence sits at position i; the sequence's
+ *     current (query) token sits at position seq_len - 1, so decode attends
+ *     to rows 0..seq_len-1 (the causal mask of section 03 of "How DeepSeek
+ *     Rewrote the Transformer (MLA)" for the newest row, section 04).
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* mla_stream_t; /* same object as cudaStream_t */
+
+typedef enum mla_status {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1, /* bad pointer, size, or configuration value        */
+    MLA_ERR_UNSUPPORTED = 2, /* valid, but a shape/dtype this build cannot run   */
+    MLA_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small       */
+    MLA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed             */
+    MLA_ERR_TIMEOUT = 5,     /* device: a bounded wait in a kernel gave up       */
+    MLA_ERR_INDEX = 6        /* device: a block id or sequence index was invalid */
+} mla_status;
+
+typedef enum mla_dtype { MLA_DTYPE_BF16 = 0, MLA_DTYPE_F32 = 1 } mla_dtype;
+
+/*
+ * Shapes and parameters of one MLA layer.
+ *   heads       H, number of attention heads (128 for DeepSeek-V2 shapes)
+ *   d_latent    d_L, latent width shared by keys and values (512)
+ *   d_rope      d_R, decoupled rotary key/query width, even (64)
+ *   d_nope      d_n, per-head query/key width on the latent side (128)
+ *   d_v         per-head value width (128)
+ *   block_size  tokens per cache page
+ *   dtype       element type of cache, queries, weights and outputs
+ *   softmax_scale  multiplies q.k before the softmax ("divide by the square
+ *               root of the dimension": 1/sqrt(d_n + d_R) is the usual value)
+ *   rope_base   base of the rotary frequencies theta_j = rope_base^(-2j/d_R)
+ *               (rotation of interleaved pairs (2j, 2j+1) by pos * theta_j)
+ */
+typedef struct mla_config {
+    int heads;
+    int d_latent;
+    int d_rope;
+    int d_nope;
+    int d_v;
+    int block_size;
+    int dtype;
+    float softmax_scale;
+    double rope_base;
+} mla_config;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mla_status_string(int status);
+
+/* Library ABI version: MAJOR * 10000 + MINOR * 100 + PATCH. */
+int mla_version(void);
+
+/*
+ * Which decode kernel mla_decode runs for `cfg`: 1 = tensor-core kernel
+ * (tcgen05/TMEM, TMA-fed), 0 = CUDA-core kernel (fp32 FMA; fp32 configs and
+ * shapes the tensor-core kernel does not take), -1 = invalid config.
+ */
+int mla_decode_path(const mla_config* cfg);
+
+/*
+ * Reads and clears the current device's status word (see above).  Waits for
+ * `stream` to finish first.  *out receives MLA_OK or the first device-side
+ * error recorded since the last call.
+ */
+int mla_get_status(mla_stream_t stream, int* out);
+
+/*
+ * Down-projects new tokens into cache rows and writes them to their paged
+ * slots ("The construction": L = X W_L; "The RoPE problem": the rotary part
+ * is kept apart from the latent; "How DeepSeek Rewrote the Transformer
+ * (MLA)", section 04: appending leaves every earlier row untouched).
+ *   x            [n_tok][d_in]                   hidden states of the new tokens
+ *   w_dkv        [d_in][d_latent + d_rope]       [W_L | W_KR]
+ *   seq_idx      [n_tok] int32                   sequence of each token, in [0, batch)
+ *   pos          [n_tok] int32                   position of each token in its sequence
+ *   block_table  [batch][max_blocks] int32
+ *   cache        [num_blocks][block_size][d_latent + d_rope]   (written)
+ *   dense_out    [n_tok][d_latent + d_rope] or NULL: also receives each row,
+ *                bit-identical to what is written into the cache
+ * Row t = [x_t W_L | RoPE(x_t W_KR, pos_t)], accumulated in fp32, rotary
+ * angles in fp64, rounded once to dtype.  Tokens whose slot is invalid are
+ * skipped and flagged MLA_ERR_INDEX on the device.
+ */
+int mla_append_latent(const mla_config* cfg, const void* x, int n_tok, int d_in,
+                      const void* w_dkv, const int32_t* seq_idx, const int32_t* pos,
+                      const int32_t* block_table, int batch, int max_blocks, void* cache,
+                      int64_t num_blocks, void* dense_out, mla_stream_t stream);
+
+/*
+ * Query absorption, the first merge of "Two merges are where the compute win
+ * comes from" (section of "Multi-Head Latent Attention (MLA)"):
+ *   q_lat[b][h][:] = q_nope[b][h][:] . W_LK_h^T
+ *   q_nope  [batch][heads][d_nope]
+ *   w_uk    [heads][d_latent][d_nope]   W_LK_h maps a latent to the head's key
+ *   q_lat   [batch][heads][d_latent]    (written; fp32 accumulation)
+ */
+int mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* w_uk, int batch,
+                 void* q_lat, mla_stream_t stream);
+
+/*
+ * Bytes of scratch that mla_decode needs for `batch` sequences on the current
+ * device (split-KV partial results).  The size depends only on the config,
+ * the batch and the device, never on sequence lengths.
+ */
+int mla_decode_workspace_size(const mla_config* cfg, int batch, size_t* bytes);
+
+/*
+ * Absorbed decode attention over the shared latent cache, for one new query
+ * token per sequence (section 03 steps of "How DeepSeek Rewrote the
+ * Transformer (MLA)" applied in latent space; section 04: only the newest
+ * query row is computed).
+ *   q_lat        [batch][heads][d_latent]   absorbed query (mla_absorb_q)
+ *   q_pe         [batch][heads][d_rope]     rotary query part, already rotated
+ *   cache        [num_blocks][block_size][d_latent + d_rope]
+ *   block_table  [batch][max_blocks] int32
+ *   seq_lens     [batch] int32, attended tokens incl. the current one, >= 1
+ *   o_lat        [batch][heads][d_latent]   (written) sum_i p_i c_i
+ *   lse          [batch][heads] float32 or NULL: natural-log log-sum-exp of
+ *                the scaled scores
+ *   workspace    >= mla_decode_workspace_size() bytes, 256-byte aligned
+ * The context is split into ranges that keep every SM busy; each range
+ * yields a partial (o, lse) pair that a combine kernel merges.  The result
+ * does not depend on how the ranges fall, up to rounding.
+ */
+int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const void* cache,
+               int64_t num_blocks, const int32_t* block_table, int max_blocks,
+               const int32_t* seq_lens, int batch, void* o_lat, float* lse, void* workspace,
+               size_t ws_bytes, mla_stream_t stream);
+
+/*
+ * Merges partial decode results computed over disjoint token ranges of the
+ * same sequences (e.g. ranges held by different devices):
+ *   LSE = log sum_s exp(lse_s),  o = sum_s exp(lse_s - LSE) o_s.
+ *   o_part    [n_splits][batch][heads][d_latent] float32
+ *   lse_part  [n_splits][batch][heads] float32; -inf marks an empty range
+ *   o_lat     [batch][heads][d_latent] (written, dtype); all-empty rows give 0
+ *   lse       [batch][heads] float32 or NULL (written)
+ */
+int mla_decode_combine(const mla_config* cfg, const float* o_part, const float* lse_part,
+                       int n_splits, int batch, void* o_lat, float* lse, mla_stream_t stream);
+
+/*
+ * Output side, the second merge: o_v[b][h] = o_lat[b][h] . W_LV_h, then
+ * out[b] = concat_h(o_v[b][h]) . W_O (section 03: stack the heads and
+ * multiply by W_O).
+ *   o_lat  [batch][heads][d_latent]
+ *   w_uv   [heads][d_latent][d_v]
+ *   o_v    [batch][heads][d_v]             (written)
+ *   w_o    [heads * d_v][d_model] or NULL  (then `out` is not written)
+ *   out    [batch][d_model]                (written when w_o != NULL)
+ */
+int mla_project_out(const mla_config* cfg, const void* o_lat, const void* w_uv, int batch,
+                    void* o_v, const void* w_o, int d_model, void* out, mla_stream_t stream);
+
+/*
+ * Query of the current tokens ("Latent Space Strikes Again", "The Core
+ * Idea": optional query compression; "Multi-Head Latent Attention (MLA)":
+ * W_Q = W_LQ W_LQQ plus a rotary query part per head):
+ *   c_q = x W_DQ (skipped when w_dq == NULL: c_q = x)
+ *   [q_nope_h | r_h] = c_q W_UQ_h,  q_pe_h = RoPE(r_h, pos_b)
+ *   x       [batch][d_in]
+ *   w_dq    [d_in][d_lq] or NULL
+ *   w_uq    [d_q][heads][d_nope + d_rope]   d_q = d_lq, or d_in without w_dq
+ *   pos     [batch] int32
+ *   q_nope  [batch][heads][d_nope], q_pe [batch][heads][d_rope]  (written)
+ *   scratch >= mla_query_proj_workspace_size() bytes, 256-byte aligned
+ */
+int mla_query_proj_workspace_size(const mla_config* cfg, int batch, int d_lq, size_t* bytes);
+int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, const void* w_dq,
+                   int d_lq, const void* w_uq, const int32_t* pos, void* q_nope, void* q_pe,
+                   void* scratch, size_t scratch_bytes, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

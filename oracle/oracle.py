@@ -231,15 +231,17 @@ def reference_cached_decode(w, pairs=None, plant=PLANT_NONE):
                   w["w_uk"], w["w_uv"], w["scale"], pairs=pairs, plant=plant)
 
 
-def reference_token_decode(w, pairs=None, plant=PLANT_NONE):
+def reference_token_decode(w, pairs=None, seqs=None, plant=PLANT_NONE):
     """Decode step for workloads that carry the current tokens' hidden states x.
 
-    1. the current token's cache row = [x W_L | RoPE(x W_KR, pos)] written at
-       its slot (earlier rows come from the given cache);
-    2. query = x (W_LQ) W_UQ per head, rotary part at pos;
+    1. each new token's cache row = [x W_L | RoPE(x W_KR, pos)] written at its
+       slot (earlier rows come from the given cache);
+    2. query = x (W_LQ) W_UQ per head, rotary part at the query position;
     3. unmerged attention over all seq_len rows; 4. stack heads, multiply by W_O.
-    Returns the decode dict plus "cache" (the cache after the append) and the
-    new rows.
+    seqs: restrict steps 2-4 to these sequences (results are indexed by
+    position in `seqs`); pairs: (index into seqs, head) pairs, as in decode().
+    Returns the decode dict plus "cache" (after the append), the new rows and
+    the queries.
     """
     cfg = w["cfg"]
     d_l, d_r = cfg["d_latent"], cfg["d_rope"]
@@ -254,11 +256,16 @@ def reference_token_decode(w, pairs=None, plant=PLANT_NONE):
     for t in range(rows.shape[0]):
         s = slot(w["block_table"], bs, nb, int(w["seq_idx_new"][t]), int(w["pos_new"][t]))
         flat[s] = stored[t]
-    q_nope, q_pe = query(w["x_q"], w["w_uq"], cfg["heads"], cfg["d_nope"], d_r, w["pos_q"],
+    B = w["block_table"].shape[0]
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    bt = np.asarray(w["block_table"])[seqs]
+    sl = np.asarray(w["seq_lens"])[seqs]
+    x_q = np.asarray(w["x_q"])[seqs]
+    pos_q = np.asarray(w["pos_q"])[seqs]
+    q_nope, q_pe = query(x_q, w["w_uq"], cfg["heads"], cfg["d_nope"], d_r, pos_q,
                          w_dq=w.get("w_dq"), base=base)
-    res = decode(cache, w["block_table"], w["seq_lens"], q_nope, q_pe, w["w_uk"], w["w_uv"],
-                 w["scale"], w_o=w.get("w_o") if pairs is None else None, pairs=pairs,
-                 plant=plant)
+    res = decode(cache, bt, sl, q_nope, q_pe, w["w_uk"], w["w_uv"], w["scale"],
+                 w_o=w.get("w_o") if pairs is None else None, pairs=pairs, plant=plant)
     res["cache"] = cache
     res["rows"] = rows
     res["q_nope"] = q_nope

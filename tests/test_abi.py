@@ -1,0 +1,80 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry
+point, and rejects invalid arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from head_latent_attention_23_b300 import build_lib, mla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return mla.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(mla.EXPORTS) == names
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert mla.status_string(code) not in ("", "unknown status")
+    assert mla.status_string(99) == "unknown status"
+    assert L.mla_version() >= 100
+
+
+def test_invalid_configs_are_rejected_on_the_host(L):
+    n = ctypes.c_size_t(0)
+    assert L.mla_decode_workspace_size(None, 4, ctypes.byref(n)) == mla.MLA_ERR_INVALID_ARG
+    assert L.mla_decode_path(None) == -1
+    good = mla.config(128, 512, 64, 128, 128, 64, "bf16")
+    bad = [
+        dict(heads=0), dict(d_rope=63), dict(d_latent=0), dict(block_size=0), dict(dtype=7),
+        dict(softmax_scale=float("nan")), dict(rope_base=-1.0), dict(d_nope=0),
+    ]
+    for kw in bad:
+        c = mla.Config.from_buffer_copy(good)
+        for k, v in kw.items():
+            setattr(c, k, v)
+        assert L.mla_decode_path(ctypes.byref(c)) == -1, kw
+        assert L.mla_decode_workspace_size(ctypes.byref(c), 4, ctypes.byref(n)) == \
+            mla.MLA_ERR_INVALID_ARG, kw
+        assert L.mla_absorb_q(ctypes.byref(c), None, None, 1, None, None) == \
+            mla.MLA_ERR_INVALID_ARG, kw
+
+
+def test_bad_sizes_and_null_pointers_are_rejected(L):
+    c = mla.config(128, 512, 64, 128, 128, 64, "bf16")
+    cp = ctypes.byref(c)
+    # batch out of range, null pointers: rejected before any CUDA call
+    assert L.mla_decode(cp, None, None, None, 1, None, 1, None, 0, None, None, None, 0,
+                        None) == mla.MLA_ERR_INVALID_ARG
+    assert L.mla_decode(cp, None, None, None, 1, None, 1, None, 2, None, None, None, 0,
+                        None) == mla.MLA_ERR_INVALID_ARG
+    assert L.mla_decode_combine(cp, None, None, 0, 1, None, None, None) == \
+        mla.MLA_ERR_INVALID_ARG
+    assert L.mla_decode_combine(cp, None, None, 2000, 1, None, None, None) == \
+        mla.MLA_ERR_INVALID_ARG
+    assert L.mla_append_latent(cp, None, 1, 0, None, None, None, None, 1, 1, None, 1, None,
+                               None) == mla.MLA_ERR_INVALID_ARG
+    assert L.mla_append_latent(cp, None, 0, 16, None, None, None, None, 1, 1, None, 1, None,
+                               None) == mla.MLA_OK          # nothing to append
+    assert L.mla_project_out(cp, None, None, 2, None, None, 0, None, None) == \
+        mla.MLA_ERR_INVALID_ARG
+    assert L.mla_query_proj(cp, None, 2, 16, None, 0, None, None, None, None, None, 0,
+                            None) == mla.MLA_ERR_INVALID_ARG

@@ -1,0 +1,221 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Metric: max|gpu - ref| / max|ref| over a whole tensor (or over the sampled
+rows at full size).  Bars: 5e-3 for bf16 inputs with fp32 accumulation, 1e-5
+for fp32.  Cache indexing (which slots the append writes) is bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from head_latent_attention_23_b300 import mla, workloads as W
+from head_latent_attention_23_b300.runner import DecodeStep
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 5e-3, "f32": 1e-5}
+
+
+def rel(gpu, ref):
+    g = np.asarray(gpu, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    assert np.isfinite(g).all()
+    return float(np.max(np.abs(g - r)) / max(np.max(np.abs(r)), 1e-30))
+
+
+def host(t):
+    return t.detach().float().cpu().numpy()
+
+
+def run_step(w):
+    step = DecodeStep(w)
+    step.run()
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK
+    return step
+
+
+def check_pairs(step, ref, pairs, tol):
+    res = step.results()
+    for key in ("o_lat", "o_v"):
+        g = np.stack([host(res[key][b, h]) for b, h in pairs])
+        r = np.stack([ref[key][b, h] for b, h in pairs])
+        assert rel(g, r) <= tol, key
+    g = np.array([float(res["lse"][b, h]) for b, h in pairs])
+    r = np.array([ref["lse"][b, h] for b, h in pairs])
+    assert rel(g, r) <= tol, "lse"
+
+
+# ---------------------------------------------------------------- small cases
+
+def test_tiny_f32_full_step():
+    """fp32, 8 heads, 128 tokens appended from x, one query: every output."""
+    w = W.tiny_f32()
+    step = run_step(w)
+    ref = O.reference_token_decode(W.oracle_view(w))
+    tol = TOL["f32"]
+    res = step.results()
+    assert rel(host(step.cache).reshape(-1, 80)[:128], ref["rows"]) <= tol
+    assert rel(host(res["q_nope"]), ref["q_nope"]) <= tol
+    assert rel(host(res["q_pe"]), ref["q_pe"]) <= tol
+    for key in ("o_lat", "o_v", "lse", "out"):
+        assert rel(host(res[key]), ref[key]) <= tol, key
+
+
+@pytest.mark.parametrize("lens,permute", [([1, 63, 64, 65, 200, 1000], True),
+                                          ([129, 4, 777], False)])
+def test_decode_small_ragged_bf16(lens, permute):
+    """DeepSeek-V2 head/latent shapes, ragged lengths around the 64-token tile
+    and page boundaries, all (sequence, head) pairs."""
+    w = W.cached_decode(len(lens), lens, seed=11, permute=permute)
+    step = run_step(w)
+    ref = O.reference_cached_decode(W.oracle_view(w))
+    res = step.results()
+    for key in ("o_lat", "o_v", "lse"):
+        assert rel(host(res[key]), ref[key]) <= TOL["bf16"], key
+
+
+def test_seq_len_one_returns_the_cached_latent():
+    w = W.cached_decode(3, [1, 1, 1], seed=5, permute=True)
+    step = run_step(w)
+    c = w["cache"].float().numpy()
+    bt = w["block_table"].numpy()
+    o = host(step.o_lat)
+    for b in range(3):
+        row = c[bt[b, 0], 0, :512]
+        assert np.array_equal(o[b], np.broadcast_to(row, o[b].shape))
+
+
+def test_masked_slots_do_not_leak():
+    """Rows after seq_len in the last page hold huge values; they must not
+    change the result."""
+    w = W.cached_decode(2, [70, 5], seed=6)
+    a = run_step(w)
+    o1 = host(a.o_lat).copy()
+    bt = w["block_table"].numpy()
+    w["cache"][bt[0, 1], 6:] = 1e4
+    w["cache"][bt[1, 0], 5:] = -1e4
+    b = run_step(w)
+    assert np.array_equal(o1, host(b.o_lat))
+
+
+def test_append_indexing_is_bit_exact():
+    """The append's rows scattered by the oracle's index map reproduce the GPU
+    cache byte for byte; every other slot keeps its canary."""
+    for dtype, tol in (("bf16", TOL["bf16"]), ("f32", TOL["f32"])):
+        g = torch.Generator().manual_seed(3)
+        cfg = mla.config(128, 512, 64, 128, 128, 64, dtype)
+        td = W.torch_dtype(dtype)
+        nb, B, maxb, n_tok, d_in = 12, 3, 4, 40, 320
+        bt = torch.randperm(nb, generator=g)[:B * maxb].reshape(B, maxb).to(torch.int32)
+        seq_idx = torch.randint(0, B, (n_tok,), generator=g).to(torch.int32)
+        pos = torch.randint(0, maxb * 64, (n_tok,), generator=g).to(torch.int32)
+        # distinct (seq, pos) so no two tokens target the same slot
+        key = seq_idx.long() * 100000 + pos.long()
+        keep = torch.unique(key, return_inverse=False)
+        seq_idx = (keep // 100000).to(torch.int32)
+        pos = (keep % 100000).to(torch.int32)
+        n_tok = seq_idx.numel()
+        x = torch.randn(n_tok, d_in, generator=g).to(td)
+        w_dkv = (torch.randn(d_in, 576, generator=g) / d_in ** 0.5).to(td)
+        canary = torch.full((nb, 64, 576), 7.25, dtype=td)
+        cache = canary.cuda()
+        dense = torch.empty((n_tok, 576), dtype=td, device="cuda")
+        mla.append_latent(cfg, x.cuda(), w_dkv.cuda(), seq_idx.cuda(), pos.cuda(), bt.cuda(),
+                          cache, dense)
+        torch.cuda.synchronize()
+        assert mla.get_status() == mla.MLA_OK
+        esz = 2 if dtype == "bf16" else 4
+        expect = canary.view(torch.uint8).numpy().reshape(nb * 64, 576 * esz).copy()
+        rows_u8 = dense.cpu().view(torch.uint8).numpy().reshape(n_tok, 576 * esz)
+        assert O.scatter_rows(rows_u8, seq_idx.numpy(), pos.numpy(), bt.numpy(), 64,
+                              expect) == 0
+        got = cache.cpu().view(torch.uint8).numpy().reshape(nb * 64, 576 * esz)
+        assert np.array_equal(got, expect)
+        ref = O.latent_rows(x.float().numpy(), w_dkv.float().numpy(), 512, 64, pos.numpy())
+        assert rel(dense.float().cpu().numpy(), ref) <= tol
+
+
+def test_invalid_block_id_is_flagged_not_read():
+    w = W.cached_decode(2, [100, 100], seed=8)
+    w["block_table"][1, 1] = 10 ** 6
+    step = DecodeStep(w)
+    step.run()
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_ERR_INDEX
+    assert mla.get_status() == mla.MLA_OK          # reading clears it
+    # the intact sequence is still right
+    ref = O.reference_cached_decode(W.oracle_view(W.cached_decode(2, [100, 100], seed=8)),
+                                    pairs=[(0, h) for h in range(128)])
+    assert rel(host(step.o_lat[0]), ref["o_lat"][0]) <= TOL["bf16"]
+
+
+def test_combine_of_oracle_partials_equals_full_attention():
+    """Two page-aligned token ranges decoded separately by the oracle, merged
+    by mla_decode_combine, equal the oracle over the whole sequence.  A third,
+    empty range (lse = -inf) must not contribute."""
+    w = W.cached_decode(2, [256, 192], seed=9)
+    v = W.oracle_view(w)
+    full = O.reference_cached_decode(v)
+    bt = v["block_table"]
+    parts = []
+    for lo_page, hi_page in ((0, 2), (2, 4)):
+        sub_bt = np.full_like(bt, -1)
+        lens = []
+        for b in range(2):
+            n_pages = (int(v["seq_lens"][b]) + 63) // 64
+            hp = min(hi_page, n_pages)
+            sub_bt[b, :hp - lo_page] = bt[b, lo_page:hp]
+            lens.append(min(int(v["seq_lens"][b]), hp * 64) - lo_page * 64)
+        parts.append(O.decode(v["cache"], sub_bt, lens, v["q_nope"], v["q_pe"], v["w_uk"],
+                              v["w_uv"], v["scale"]))
+    o_part = np.stack([p["o_lat"] for p in parts] + [np.zeros_like(parts[0]["o_lat"])])
+    lse_part = np.stack([p["lse"] for p in parts] + [np.full_like(parts[0]["lse"], -np.inf)])
+    cfg = mla.config_from(w["cfg"])
+    o_lat = torch.empty((2, 128, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((2, 128), dtype=torch.float32, device="cuda")
+    mla.decode_combine(cfg, torch.from_numpy(o_part).float().cuda(),
+                       torch.from_numpy(lse_part).float().cuda(), o_lat, lse)
+    torch.cuda.synchronize()
+    assert rel(host(o_lat), full["o_lat"]) <= TOL["bf16"]
+    assert rel(host(lse), full["lse"]) <= 1e-5
+
+
+# ---------------------------------------------------------------- full size
+
+def _pairs(B, H, seed, k=6):
+    r = np.random.default_rng(seed)
+    ps = {(0, 0), (B - 1, H - 1)}
+    while len(ps) < k:
+        ps.add((int(r.integers(B)), int(r.integers(H))))
+    return sorted(ps)
+
+
+@pytest.mark.parametrize("name", ["v2_b16_ctx4k", "v2_ragged_b64", "v2_long_b4_ctx100k"])
+def test_full_size_cached_workloads_sampled(name):
+    w = W.WORKLOADS[name]()
+    step = run_step(w)
+    pairs = _pairs(w["batch"], 128, 1)
+    ref = O.reference_cached_decode(W.oracle_view(w), pairs=pairs)
+    check_pairs(step, ref, pairs, TOL["bf16"])
+
+
+def test_full_layer_step_sampled():
+    """hidden 7168 -> latent + rotary append, query latent 1536, 128 heads,
+    batch 128, contexts 2048; out = W_O projection of all heads of one
+    sequence, plus sampled (sequence, head) pairs."""
+    w = W.v2_layer_b128_ctx2k()
+    step = run_step(w)
+    v = W.oracle_view(w)
+    seqs = [0, 77]
+    ref = O.reference_token_decode(v, seqs=[77])
+    assert rel(host(step.out[77]), ref["out"][0]) <= TOL["bf16"]
+    pairs = [(0, 0), (0, 127), (1, 5), (1, 64)]
+    ref2 = O.reference_token_decode(v, seqs=seqs, pairs=pairs)
+    res = step.results()
+    for key in ("o_lat", "o_v"):
+        g = np.stack([host(res[key][seqs[i], h]) for i, h in pairs])
+        r = np.stack([ref2[key][i, h] for i, h in pairs])
+        assert rel(g, r) <= TOL["bf16"], key
