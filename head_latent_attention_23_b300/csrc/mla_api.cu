@@ -288,3 +288,74 @@ int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, co
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory where they decode: a host
+// framework that owns every byte of device memory through its own pool and
+// forbids direct cudaMalloc, a plugin interface that passes only input and
+// output pointers, or a latency-critical loop where an allocation's implicit
+// device synchronisation is not acceptable.  For them the split-KV partial
+// results live in the fixed static array below instead of a workspace.  Every
+// GPU that loads this library holds the array until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices];
+
+// Device address of the static array for the current device, looked up once
+// per device with that device current.
+int noalloc_scratch(void** out) {
+    int dev;
+    if (int rc = current_device(&dev)) return rc;
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return MLA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" int mla_decode_noalloc(const mla_config* cfg, const void* q_lat, const void* q_pe,
+                                  const void* cache, int64_t num_blocks,
+                                  const int32_t* block_table, int max_blocks,
+                                  const int32_t* seq_lens, int batch, void* o_lat, float* lse,
+                                  mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (batch < 1 || batch > kMaxDecodeBatch || max_blocks < 1 || num_blocks < 1)
+        return MLA_ERR_INVALID_ARG;
+    if ((int64_t)max_blocks * cfg->block_size > (int64_t)1 << 30) return MLA_ERR_INVALID_ARG;
+    if (!q_lat || (!q_pe && cfg->d_rope > 0) || !cache || !block_table || !seq_lens || !o_lat)
+        return MLA_ERR_INVALID_ARG;
+    // The partials of W workers need (W + batch) slots; use as many workers
+    // as the array holds, up to the count mla_decode would use.
+    int W;
+    if (int rc = decode_workers(cfg, &W)) return rc;
+    while (W >= 1 && decode_ws_bytes(cfg, W, batch) > MLA_NOALLOC_SCRATCH_BYTES) --W;
+    if (W < 1) return MLA_ERR_UNSUPPORTED;
+    void* scratch;
+    if (int rc = noalloc_scratch(&scratch)) return rc;
+    int* status;
+    if (int rc = status_ptr(&status)) return rc;
+    // Nothing in the array has to start at zero: every partial slot the
+    // merge reads is written earlier in the same call.
+    const size_t slots = (size_t)W + batch;
+    DecodeArgs a{};
+    a.heads = cfg->heads; a.d_latent = cfg->d_latent; a.d_rope = cfg->d_rope;
+    a.block_size = cfg->block_size; a.max_blocks = max_blocks; a.batch = batch;
+    a.workers = W; a.num_blocks = num_blocks; a.scale = cfg->softmax_scale;
+    a.q_lat = q_lat; a.q_pe = q_pe; a.cache = cache; a.block_table = block_table;
+    a.seq_lens = seq_lens; a.o_lat = o_lat; a.lse = lse; a.status = status;
+    a.o_part = (float*)scratch;
+    a.lse_part = (float*)((char*)scratch +
+                          align256(slots * cfg->heads * cfg->d_latent * sizeof(float)));
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = use_tc(cfg) ? launch_decode_tc(a, st) : launch_decode_simt(a, cfg->dtype, st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    return cuda_rc(launch_combine_planned(a, cfg->dtype, st));
+}

@@ -31,6 +31,7 @@ EXPORTS = (
     "mla_status_string", "mla_version", "mla_decode_path", "mla_get_status",
     "mla_append_latent", "mla_absorb_q", "mla_decode_workspace_size", "mla_decode",
     "mla_decode_combine", "mla_project_out", "mla_query_proj_workspace_size", "mla_query_proj",
+    "mla_decode_noalloc",
 )
 
 
@@ -93,6 +94,7 @@ def lib():
         L.mla_project_out.argtypes = [CP, P, P, I, P, P, I, P, P]
         L.mla_query_proj_workspace_size.argtypes = [CP, I, I, SZ]
         L.mla_query_proj.argtypes = [CP, P, I, I, P, I, P, P, P, P, P, ctypes.c_size_t, P]
+        L.mla_decode_noalloc.argtypes = [CP, P, P, P, I64, P, I, P, I, P, P, P]
         for name in EXPORTS:
             if name not in ("mla_status_string", "mla_version"):
                 getattr(L, name).restype = I
@@ -189,6 +191,21 @@ def decode(cfg, q_lat, q_pe, cache, block_table, seq_lens, o_lat, lse=None, work
         _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "mla_decode")
+
+
+def decode_noalloc(cfg, q_lat, q_pe, cache, block_table, seq_lens, o_lat, lse=None,
+                   stream=None):
+    """mla_decode_noalloc: mla_decode with its partials in the library's static
+    device array instead of a caller workspace (for callers that cannot
+    allocate).  Calls on one device must not overlap on the GPU."""
+    dt = _tdtype(cfg)
+    batch, max_blocks = block_table.shape
+    rc = lib().mla_decode_noalloc(
+        ctypes.byref(cfg), _ptr(q_lat, dt, "q_lat"), _ptr(q_pe, dt, "q_pe"),
+        _ptr(cache, dt, "cache"), cache.shape[0], _ptr(block_table, torch.int32, "block_table"),
+        max_blocks, _ptr(seq_lens, torch.int32, "seq_lens"), batch, _ptr(o_lat, dt, "o_lat"),
+        _ptr(lse, torch.float32, "lse"), _stream(stream))
+    _check(rc, "mla_decode_noalloc")
 
 
 def decode_combine(cfg, o_part, lse_part, o_lat, lse=None, stream=None):

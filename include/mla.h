@@ -219,6 +219,36 @@ int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, co
                    int d_lq, const void* w_uq, const int32_t* pos, void* q_nope, void* q_pe,
                    void* scratch, size_t scratch_bytes, mla_stream_t stream);
 
+/*
+ * mla_decode without a workspace argument: the split-KV partial results go to
+ * a static device array of MLA_NOALLOC_SCRATCH_BYTES that the library itself
+ * holds on every GPU that loads it, until the process exits.  The pages
+ * describe no such call; it exists for callers that cannot allocate device
+ * memory at the point where they decode (a framework that owns all device
+ * memory through its own pool and forbids direct cudaMalloc, a plugin
+ * interface that passes only inputs and outputs, or a latency-critical loop
+ * where an allocation's implicit device synchronisation is not allowed).
+ *
+ * Arguments and results are those of mla_decode.  The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *   - Limit: the array must hold the partials of at least one worker plus one
+ *     per sequence: (1 + batch) * heads * (d_latent + 1) * 4 bytes, rounded
+ *     up to 256-byte regions.  Larger requests return MLA_ERR_UNSUPPORTED and
+ *     launch nothing.  When the array is smaller than what mla_decode would
+ *     use, the context is split into fewer ranges (same result up to rounding).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its partials
+ *     there.  Nothing in it has to start at zero.  Calls that overlap on the
+ *     GPU (concurrent streams, or several host threads) race on the array and
+ *     give wrong results: serialise them.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int mla_decode_noalloc(const mla_config* cfg, const void* q_lat, const void* q_pe,
+                       const void* cache, int64_t num_blocks, const int32_t* block_table,
+                       int max_blocks, const int32_t* seq_lens, int batch, void* o_lat,
+                       float* lse, mla_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
