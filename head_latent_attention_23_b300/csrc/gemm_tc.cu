@@ -1,0 +1,210 @@
+// Tensor-core GEMM for the projections around the attention core (bf16
+// operands, fp32 accumulation in TMEM): the query up-projection and its
+// absorption into latent space (first merge), the value/output projections
+// (second merge) and the cache append's down-projection, whose epilogue
+// applies RoPE and scatters rows into the paged cache.
+//
+//   C[z][m][n] = sum_k A[z][m][k] * B[z][k][n]
+//
+// One CTA computes a 128 x 128 tile of C.  Warp 0 streams 64-deep k slices
+// of A (K-major) and B (K-major or N-major) into a 4-stage ring with TMA
+// (128-byte swizzle); one thread of warp 1 issues tcgen05.mma (M=128, N=128,
+// K=16) into a TMEM accumulator; warps 2-5 drain TMEM through registers.
+#include "kernels.h"
+#include "tc_ptx.cuh"
+#include "tmap.h"
+
+namespace mla {
+
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kBK = 64, kStages = 4;
+constexpr int kTileBytes = 16384;   // one 128 x 64 bf16 slice of A or of B
+constexpr int kSmemBytes = 1024 + kStages * 2 * kTileBytes + 256;
+
+using namespace tc;
+
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                   const TcGemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kTileBytes;
+    uint64_t* full = (uint64_t*)(sB + kStages * kTileBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* done = empty + kStages;
+    uint32_t* tslot = (uint32_t*)(done + 1);
+    volatile int* abort_flag = (volatile int*)(tslot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM, z = blockIdx.z;
+    const int nk = (p.K + kBK - 1) / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tA);
+        prefetch_tmap(&tB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, kBN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int kt = 0; kt < nk; ++kt) {
+                const int s = kt % kStages;
+                if (!mbar_wait(&empty[s], ((kt / kStages) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
+                tma_load_3d(sA + s * kTileBytes, &tA, kt * kBK, m0, z, &full[s]);
+                if (p.b_mn) {
+                    tma_load_3d(sB + s * kTileBytes, &tB, n0, kt * kBK, z, &full[s]);
+                    tma_load_3d(sB + s * kTileBytes + kTileBytes / 2, &tB, n0 + 64, kt * kBK, z,
+                                &full[s]);
+                } else {
+                    tma_load_3d(sB + s * kTileBytes, &tB, kt * kBK, n0, z, &full[s]);
+                }
+                issued = kt + 1;
+            }
+            // every copy this thread started has landed before the CTA exits
+            for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt)
+                drain_wait(&full[kt % kStages], (kt / kStages) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kBM, kBN, false, p.b_mn != 0);
+            for (int kt = 0; kt < nk; ++kt) {
+                const int s = kt % kStages;
+                if (!mbar_wait(&full[s], (kt / kStages) & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + s * kTileBytes);
+                const uint32_t b0 = smem_u32(sB + s * kTileBytes);
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k) {
+                    const uint64_t ad = sdesc(a0 + 32 * k, 16, 1024, 2);
+                    const uint64_t bd = p.b_mn ? sdesc(b0 + 2048 * k, kTileBytes / 2, 1024, 2)
+                                               : sdesc(b0 + 32 * k, 16, 1024, 2);
+                    mma_ss(tmem, ad, bd, idesc, (kt | k) != 0);
+                }
+                tc_commit(&empty[s]);
+            }
+            tc_commit(done);
+            drain_wait(done, 0);
+        }
+    } else {
+        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = tile rows
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const int m = m0 + row;
+        bool ok = mbar_wait(done, 0, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+        if (ok) {
+            int64_t slot = -1;
+            if (p.epi == 1 && m < p.M) {
+                const int b = p.seq_idx[m], ps = p.pos[m];
+                if (b >= 0 && b < p.batch && ps >= 0 && ps < p.max_blocks * p.block_size) {
+                    const int32_t blk = p.block_table[(size_t)b * p.max_blocks + ps / p.block_size];
+                    if (blk >= 0 && blk < p.num_blocks)
+                        slot = (int64_t)blk * p.block_size + ps % p.block_size;
+                }
+                if (slot < 0 && n0 == 0) flag(p.status, MLA_ERR_INDEX);
+            }
+            for (int c = 0; c < kBN; c += 16) {
+                uint32_t r[16];
+                __syncwarp();
+                MLA_TMEM_LD_X16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, r);
+                tmem_ld_wait();
+                if (m >= p.M) continue;
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                const int nb = n0 + c;
+                if (p.epi == 1) {
+                    if (nb >= p.N) continue;
+                    if (nb >= p.d_latent) {
+                        const int ps = p.pos[m];
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            const int j = (nb + i - p.d_latent) / 2;
+                            const double theta = pow(p.rope_base, -2.0 * j / (double)p.d_rope);
+                            const double phi =
+                                fmod((double)ps * theta, 6.283185307179586476925286766559);
+                            double sn, cs;
+                            sincos(phi, &sn, &cs);
+                            const float x0 = v[i], x1 = v[i + 1];
+                            v[i] = x0 * (float)cs - x1 * (float)sn;
+                            v[i + 1] = x0 * (float)sn + x1 * (float)cs;
+                        }
+                    }
+                    const int D = p.N;
+                    __nv_bfloat16* dst = slot >= 0 ? p.cache + slot * D + nb : nullptr;
+                    __nv_bfloat16* dn = p.dense_out ? p.dense_out + (size_t)m * D + nb : nullptr;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const __nv_bfloat16 h = __float2bfloat16_rn(v[i]);
+                        if (dst) dst[i] = h;
+                        if (dn) dn[i] = h;
+                    }
+                } else {
+                    const int64_t base = (int64_t)z * p.sCz + (int64_t)m * p.sCm + nb;
+                    if (p.c_dtype == MLA_DTYPE_BF16) {
+                        __nv_bfloat16* C = (__nv_bfloat16*)p.C + base;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (nb + i < p.N) C[i] = __float2bfloat16_rn(v[i]);
+                    } else {
+                        float* C = (float*)p.C + base;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (nb + i < p.N) C[i] = v[i];
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kBN);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmParams& p,
+                           int batch, cudaStream_t st) {
+    if (p.M <= 0 || p.N <= 0 || p.K <= 0 || batch <= 0) return cudaErrorInvalidValue;
+    CUtensorMap ta, tb;
+    const uint32_t boxA[3] = {64, 128, 1};
+    const uint32_t boxBk[3] = {64, 128, 1};
+    const uint32_t boxBn[3] = {64, 64, 1};
+    if (!make_tmap_bf16(&ta, A.ptr, 3, A.dims, A.strides, boxA, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tb, B.ptr, 3, B.dims, B.strides, p.b_mn ? boxBn : boxBk, 128))
+        return cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid((p.N + kBN - 1) / kBN, (p.M + kBM - 1) / kBM, batch);
+    gemm_tc_kernel<<<grid, 192, kSmemBytes, st>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

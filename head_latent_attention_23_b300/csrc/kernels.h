@@ -2,6 +2,7 @@
 // kernel translation units.  Host code only; not part of the public ABI.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -33,7 +34,8 @@ size_t decode_simt_smem(const DecodeArgs& a);
 // the shapes do not fit it.
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 int decode_tc_workers(int num_sms);
-bool decode_tc_supported(int heads, int d_latent, int d_rope, int block_size, int dtype);
+bool decode_tc_supported(int heads, int d_latent, int d_rope, int block_size, int dtype,
+                         int batch);
 
 // Merge of the partials written by a decode kernel (slots g + b of plan W).
 cudaError_t launch_combine_planned(const DecodeArgs& a, int dtype, cudaStream_t st);
@@ -76,5 +78,37 @@ cudaError_t launch_gemm_simt(const GemmArgs& g, int a_dtype, int b_dtype, int c_
 cudaError_t launch_q_split_rope(const float* q_all, int batch, int heads, int d_nope,
                                 int d_rope, const int32_t* pos, double rope_base, void* q_nope,
                                 void* q_pe, int dtype, cudaStream_t st);
+
+// ---------------------------------------------------------------- tcgen05 GEMM
+// A bf16 operand seen by TMA as a 3-D array: dims[0] innermost (elements),
+// strides[i] = byte stride of dims[i+1].  A: {K, M, batch}.  B: {K, N, batch}
+// when K-major ([n][k] storage), {N, K, batch} when N-major ([k][n] storage).
+struct TcOperand {
+    const void* ptr;
+    uint64_t dims[3];
+    uint64_t strides[2];
+};
+
+struct TcGemmParams {
+    int M, N, K;
+    int b_mn;              // 1: B stored [k][n]
+    int epi;               // 0: store C; 1: cache append (RoPE + paged scatter)
+    void* C;               // epi 0: element (z, m, n) at C + z*sCz + m*sCm + n
+    int64_t sCz, sCm;
+    int c_dtype;
+    // epi 1: rows are tokens, columns [0, d_latent) latent, [d_latent, N) rotary
+    int d_latent, d_rope, block_size, max_blocks, batch;
+    int64_t num_blocks;
+    double rope_base;
+    const int32_t* seq_idx;
+    const int32_t* pos;
+    const int32_t* block_table;
+    __nv_bfloat16* cache;
+    __nv_bfloat16* dense_out;
+    int* status;
+};
+
+cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmParams& p,
+                           int batch, cudaStream_t st);
 
 }  // namespace mla

@@ -68,19 +68,39 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
 constexpr int kMaxDecodeBatch = 8192;
 
-bool use_tc(const mla_config* c) {
-    return decode_tc_supported(c->heads, c->d_latent, c->d_rope, c->block_size, c->dtype);
+bool use_tc(const mla_config* c, int batch) {
+    return decode_tc_supported(c->heads, c->d_latent, c->d_rope, c->block_size, c->dtype, batch);
 }
 
-// Split-KV worker count of the decode kernel that `c` selects.
-int decode_workers(const mla_config* c, int* W) {
+// Split-KV worker count of the decode kernel that (c, batch) selects.
+int decode_workers(const mla_config* c, int batch, int* W) {
     int sms;
     if (int rc = num_sms(&sms)) return rc;
-    *W = use_tc(c) ? decode_tc_workers(sms) : sms;
+    *W = use_tc(c, batch) ? decode_tc_workers(sms) : sms;
     return MLA_OK;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+// 3-D bf16 operand view for the tensor-core GEMM.
+TcOperand op3(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
+              uint64_t s2_bytes) {
+    TcOperand o;
+    o.ptr = ptr;
+    o.dims[0] = d0; o.dims[1] = d1; o.dims[2] = d2;
+    o.strides[0] = s1_bytes; o.strides[1] = s2_bytes;
+    return o;
+}
+
+TcGemmParams gemm_params(int M, int N, int K, bool b_mn, void* C, int64_t sCz, int64_t sCm,
+                         int c_dtype, int* status) {
+    TcGemmParams g{};
+    g.M = M; g.N = N; g.K = K; g.b_mn = b_mn ? 1 : 0; g.epi = 0;
+    g.C = C; g.sCz = sCz; g.sCm = sCm; g.c_dtype = c_dtype; g.status = status;
+    return g;
+}
 
 size_t decode_ws_bytes(const mla_config* c, int W, int batch) {
     size_t slots = (size_t)W + (size_t)batch;
@@ -125,7 +145,7 @@ int mla_get_status(mla_stream_t stream, int* out) {
 
 int mla_decode_path(const mla_config* cfg) {
     if (check_cfg(cfg)) return -1;
-    return use_tc(cfg) ? 1 : 0;
+    return use_tc(cfg, 1) ? 1 : 0;
 }
 
 int mla_append_latent(const mla_config* cfg, const void* x, int n_tok, int d_in,
@@ -142,6 +162,22 @@ int mla_append_latent(const mla_config* cfg, const void* x, int n_tok, int d_in,
         return MLA_ERR_UNSUPPORTED;
     int* status;
     if (int rc = status_ptr(&status)) return rc;
+    const int D = cfg->d_latent + cfg->d_rope;
+    if (cfg->dtype == MLA_DTYPE_BF16 && d_in % 8 == 0 && D % 8 == 0 && cfg->d_latent % 16 == 0 &&
+        al16(x) && al16(w_dkv) && al16(cache) && (!dense_out || al16(dense_out))) {
+        // rows = x . [W_L | W_KR] on the tensor cores; the epilogue rotates the
+        // rotary part and writes each row to its paged slot (and dense_out)
+        TcOperand A = op3(x, d_in, n_tok, 1, (uint64_t)d_in * 2, (uint64_t)d_in * 2 * n_tok);
+        TcOperand B = op3(w_dkv, D, d_in, 1, (uint64_t)D * 2, (uint64_t)D * 2 * d_in);
+        TcGemmParams g = gemm_params(n_tok, D, d_in, true, nullptr, 0, 0, MLA_DTYPE_BF16, status);
+        g.epi = 1;
+        g.d_latent = cfg->d_latent; g.d_rope = cfg->d_rope; g.block_size = cfg->block_size;
+        g.max_blocks = max_blocks; g.batch = batch; g.num_blocks = num_blocks;
+        g.rope_base = cfg->rope_base; g.seq_idx = seq_idx; g.pos = pos;
+        g.block_table = block_table; g.cache = (__nv_bfloat16*)cache;
+        g.dense_out = (__nv_bfloat16*)dense_out;
+        return cuda_rc(launch_gemm_tc(A, B, g, 1, (cudaStream_t)stream));
+    }
     AppendArgs a{};
     a.n_tok = n_tok; a.d_in = d_in; a.d_latent = cfg->d_latent; a.d_rope = cfg->d_rope;
     a.block_size = cfg->block_size; a.max_blocks = max_blocks; a.batch = batch;
@@ -158,20 +194,31 @@ int mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* w_uk, in
     if (batch == 0) return MLA_OK;
     if (!q_nope || !w_uk || !q_lat) return MLA_ERR_INVALID_ARG;
     const int H = cfg->heads, DL = cfg->d_latent, DN = cfg->d_nope;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cfg->dtype == MLA_DTYPE_BF16 && DN % 8 == 0 && al16(q_nope) && al16(w_uk)) {
+        int* status;
+        if (int rc = status_ptr(&status)) return rc;
+        // per head h (batch index of the GEMM): [batch x DN] . W_LK_h^T, W_LK_h = [DL][DN]
+        TcOperand A = op3(q_nope, DN, batch, H, (uint64_t)H * DN * 2, (uint64_t)DN * 2);
+        TcOperand B = op3(w_uk, DN, DL, H, (uint64_t)DN * 2, (uint64_t)DL * DN * 2);
+        TcGemmParams g = gemm_params(batch, DL, DN, false, q_lat, DL, (int64_t)H * DL,
+                                     MLA_DTYPE_BF16, status);
+        return cuda_rc(launch_gemm_tc(A, B, g, H, st));
+    }
     // per head h: q_lat[:, h, :] (batch x DL) = q_nope[:, h, :] (batch x DN) . W_LK_h^T
     GemmArgs g{};
     g.M = batch; g.N = DL; g.K = DN; g.batch = H;
     g.A = q_nope; g.sA = DN; g.sAm = (int64_t)H * DN; g.sAk = 1;
     g.B = w_uk; g.sB = (int64_t)DL * DN; g.sBk = 1; g.sBn = DN;
     g.C = q_lat; g.sC = DL; g.sCm = (int64_t)H * DL; g.sCn = 1;
-    return cuda_rc(launch_gemm_simt(g, cfg->dtype, cfg->dtype, cfg->dtype, (cudaStream_t)stream));
+    return cuda_rc(launch_gemm_simt(g, cfg->dtype, cfg->dtype, cfg->dtype, st));
 }
 
 int mla_decode_workspace_size(const mla_config* cfg, int batch, size_t* bytes) {
     if (int rc = check_cfg(cfg)) return rc;
     if (!bytes || batch < 1 || batch > kMaxDecodeBatch) return MLA_ERR_INVALID_ARG;
     int W;
-    if (int rc = decode_workers(cfg, &W)) return rc;
+    if (int rc = decode_workers(cfg, batch, &W)) return rc;
     *bytes = decode_ws_bytes(cfg, W, batch);
     return MLA_OK;
 }
@@ -187,7 +234,7 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
     if (!q_lat || (!q_pe && cfg->d_rope > 0) || !cache || !block_table || !seq_lens || !o_lat)
         return MLA_ERR_INVALID_ARG;
     int W;
-    if (int rc = decode_workers(cfg, &W)) return rc;
+    if (int rc = decode_workers(cfg, batch, &W)) return rc;
     const size_t need = decode_ws_bytes(cfg, W, batch);
     if (!workspace || ws_bytes < need || ((uintptr_t)workspace & 255)) return MLA_ERR_WORKSPACE;
     int* status;
@@ -203,7 +250,8 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
     a.lse_part = (float*)((char*)workspace +
                           align256(slots * cfg->heads * cfg->d_latent * sizeof(float)));
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = use_tc(cfg) ? launch_decode_tc(a, st) : launch_decode_simt(a, cfg->dtype, st);
+    const bool tc = use_tc(cfg, batch) && al16(q_lat) && al16(q_pe) && al16(cache);
+    cudaError_t e = tc ? launch_decode_tc(a, st) : launch_decode_simt(a, cfg->dtype, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return cuda_rc(launch_combine_planned(a, cfg->dtype, st));
 }
@@ -226,6 +274,26 @@ int mla_project_out(const mla_config* cfg, const void* o_lat, const void* w_uv, 
     if (!o_lat || !w_uv || !o_v || (w_o && !out)) return MLA_ERR_INVALID_ARG;
     const int H = cfg->heads, DL = cfg->d_latent, DV = cfg->d_v;
     cudaStream_t st = (cudaStream_t)stream;
+    const bool tc = cfg->dtype == MLA_DTYPE_BF16 && DL % 8 == 0 && DV % 8 == 0 &&
+                    (!w_o || d_model % 8 == 0) && al16(o_lat) && al16(w_uv) && al16(o_v) &&
+                    (!w_o || al16(w_o));
+    if (tc) {
+        int* status;
+        if (int rc = status_ptr(&status)) return rc;
+        // per head h: o_v[:, h, :] = o_lat[:, h, :] . W_LV_h, W_LV_h = [DL][DV] (N-major)
+        TcOperand A = op3(o_lat, DL, batch, H, (uint64_t)H * DL * 2, (uint64_t)DL * 2);
+        TcOperand B = op3(w_uv, DV, DL, H, (uint64_t)DV * 2, (uint64_t)DL * DV * 2);
+        TcGemmParams g = gemm_params(batch, DV, DL, true, o_v, DV, (int64_t)H * DV,
+                                     MLA_DTYPE_BF16, status);
+        if (int rc = cuda_rc(launch_gemm_tc(A, B, g, H, st))) return rc;
+        if (!w_o) return MLA_OK;
+        const uint64_t KO = (uint64_t)H * DV;
+        TcOperand A2 = op3(o_v, KO, batch, 1, KO * 2, KO * 2 * batch);
+        TcOperand B2 = op3(w_o, d_model, KO, 1, (uint64_t)d_model * 2, KO * d_model * 2);
+        TcGemmParams g2 = gemm_params(batch, d_model, (int)KO, true, out, 0, d_model,
+                                      MLA_DTYPE_BF16, status);
+        return cuda_rc(launch_gemm_tc(A2, B2, g2, 1, st));
+    }
     // per head h: o_v[:, h, :] (batch x DV) = o_lat[:, h, :] (batch x DL) . W_LV_h (DL x DV)
     GemmArgs g{};
     g.M = batch; g.N = DV; g.K = DL; g.batch = H;
@@ -265,6 +333,32 @@ int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, co
     cudaStream_t st = (cudaStream_t)stream;
     float* cq = (float*)scratch;
     float* q_all = (float*)((char*)scratch + align256((size_t)batch * dlq * sizeof(float)));
+    if (cfg->dtype == MLA_DTYPE_BF16 && d_in % 8 == 0 && (!w_dq || d_lq % 8 == 0) &&
+        (H * DQ) % 8 == 0 && al16(x) && al16(w_uq) && (!w_dq || al16(w_dq))) {
+        int* status;
+        if (int rc = status_ptr(&status)) return rc;
+        const void* a_in = x;
+        int k_in = d_in;
+        if (w_dq) {
+            // c_q = x . W_DQ, kept in bf16 (scratch) as the next GEMM's A operand
+            TcOperand A = op3(x, d_in, batch, 1, (uint64_t)d_in * 2, (uint64_t)d_in * 2 * batch);
+            TcOperand B = op3(w_dq, d_lq, d_in, 1, (uint64_t)d_lq * 2,
+                              (uint64_t)d_lq * 2 * d_in);
+            TcGemmParams g = gemm_params(batch, d_lq, d_in, true, cq, 0, d_lq, MLA_DTYPE_BF16,
+                                         status);
+            if (int rc = cuda_rc(launch_gemm_tc(A, B, g, 1, st))) return rc;
+            a_in = cq;
+            k_in = d_lq;
+        }
+        const uint64_t NQ = (uint64_t)H * DQ;
+        TcOperand A = op3(a_in, k_in, batch, 1, (uint64_t)k_in * 2, (uint64_t)k_in * 2 * batch);
+        TcOperand B = op3(w_uq, NQ, k_in, 1, NQ * 2, NQ * 2 * k_in);
+        TcGemmParams g = gemm_params(batch, (int)NQ, k_in, true, q_all, 0, (int64_t)NQ,
+                                     MLA_DTYPE_F32, status);
+        if (int rc = cuda_rc(launch_gemm_tc(A, B, g, 1, st))) return rc;
+        return cuda_rc(launch_q_split_rope(q_all, batch, H, cfg->d_nope, cfg->d_rope, pos,
+                                           cfg->rope_base, q_nope, q_pe, cfg->dtype, st));
+    }
     const void* a_in = x;
     int a_dtype = cfg->dtype, k_in = d_in;
     if (w_dq) {
@@ -335,7 +429,7 @@ extern "C" int mla_decode_noalloc(const mla_config* cfg, const void* q_lat, cons
     // The partials of W workers need (W + batch) slots; use as many workers
     // as the array holds, up to the count mla_decode would use.
     int W;
-    if (int rc = decode_workers(cfg, &W)) return rc;
+    if (int rc = decode_workers(cfg, batch, &W)) return rc;
     while (W >= 1 && decode_ws_bytes(cfg, W, batch) > MLA_NOALLOC_SCRATCH_BYTES) --W;
     if (W < 1) return MLA_ERR_UNSUPPORTED;
     void* scratch;
@@ -355,7 +449,8 @@ extern "C" int mla_decode_noalloc(const mla_config* cfg, const void* q_lat, cons
     a.lse_part = (float*)((char*)scratch +
                           align256(slots * cfg->heads * cfg->d_latent * sizeof(float)));
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = use_tc(cfg) ? launch_decode_tc(a, st) : launch_decode_simt(a, cfg->dtype, st);
+    const bool tc = use_tc(cfg, batch) && al16(q_lat) && al16(q_pe) && al16(cache);
+    cudaError_t e = tc ? launch_decode_tc(a, st) : launch_decode_simt(a, cfg->dtype, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return cuda_rc(launch_combine_planned(a, cfg->dtype, st));
 }
