@@ -12,8 +12,10 @@ seeded (workloads.py).  Prints one JSON line (rank 0).
 
 ours:       device-resident inputs; R replicas of every input tensor are
             rotated so consecutive steps never find their cache, queries or
-            weights in L2 (R * bytes > 2 * L2).  CUDA events on the launching
-            stream; max over ranks.  e2e: the same step preceded by pinned
+            weights in L2 (R * bytes > 2 * L2).  The steps' library calls are
+            captured once into CUDA graphs and replayed; CUDA events on the
+            launching stream time the replays (and, inside the graph, each
+            mla_decode call); max over ranks.  e2e: the same step preceded by pinned
             host -> device copies of the step's inputs and followed by a
             device -> host read of its output.
 reference:  the fp64 CPU oracle (unmerged MLA) on a bounded sample of the
@@ -306,29 +308,51 @@ def run_ours(args):
 
     K = args.steps
     if K is None:
-        t0 = time.perf_counter()
-        for i in range(10):
-            steps[i % R].run()
+        # about 1.5 s of timed steps, from one replay of a 50-step graph
+        probe = capture([steps[i % R] for i in range(50)], None)
+        probe.replay()
         torch.cuda.synchronize()
-        per = (time.perf_counter() - t0) / 10
-        K = int(min(max(2.0 / per, 50), 20000))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        probe.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per = a.elapsed_time(b) / 50 / 1e3
+        K = int(min(max(1.5 / per, 200), 50000))
+        del probe
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
+    # The timed region replays CUDA graphs of whole steps (the library's
+    # kernels, captured once), so the host's per-call overhead does not leave
+    # the GPU idle between steps.  Graph A holds G consecutive steps (replicas
+    # rotated), each mla_decode call bracketed by timing events; graph B holds
+    # the remaining K mod G steps.
+    G = min(K, 500)
+    ga_steps = [steps[i % R] for i in range(G)]
+    rem = K - (K // G) * G
+    dec_ev = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(G)]
+    graph_a = capture(ga_steps, dec_ev)
+    graph_b = capture([steps[i % R] for i in range(rem)], None) if rem else None
+    for _ in range(2):           # graph warm-up (first replays upload the graph)
+        graph_a.replay()
+    torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         start.record(stream)
-        for i in range(K):
-            _run_with_decode_events(steps[i % R], ev[i], stream)
+        for _ in range(K // G):
+            graph_a.replay()
+        if graph_b is not None:
+            graph_b.replay()
         end.record(stream)
         torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     total_ms = start.elapsed_time(end)
-    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    # the last replay of graph A: one duration per mla_decode call
+    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
     if ws > 1:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -389,6 +413,9 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K * steps[0].kernels_per_step(),
+        "timing": (f"CUDA graphs of {G} steps replayed {K // G} times"
+                   + (f" + one of {rem} steps" if rem else "")
+                   + "; mla_decode durations from events inside the last replay"),
         "clocks": clk.summary(),
     }
     print(json.dumps(out), flush=True)
@@ -396,8 +423,25 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def capture(step_list, ev_pairs):
+    """A CUDA graph of the given steps' library calls, in order; with
+    ev_pairs, timing events around each mla_decode call."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        # capture-time allocations: none (every buffer is owned by a step)
+        with torch.cuda.graph(g, stream=side):
+            cs = torch.cuda.current_stream()
+            for j, s in enumerate(step_list):
+                _run_with_decode_events(s, ev_pairs[j] if ev_pairs else None, cs)
+    torch.cuda.current_stream().wait_stream(side)
+    return g
+
+
 def _run_with_decode_events(s, evpair, stream):
-    """One step with CUDA events around its mla_decode call."""
+    """One step, with CUDA events around its mla_decode call when evpair is
+    given."""
     from head_latent_attention_23_b300 import mla
     if s.kind == "token":
         mla.query_proj(s.cfg, s.x_q, s.w_uq, s.pos_q, s.q_nope, s.q_pe, w_dq=s.w_dq,
@@ -405,9 +449,11 @@ def _run_with_decode_events(s, evpair, stream):
         mla.append_latent(s.cfg, s.x_new, s.w_dkv, s.seq_idx_new, s.pos_new, s.block_table,
                           s.cache)
     mla.absorb_q(s.cfg, s.q_nope, s.w_uk, s.q_lat)
-    evpair[0].record(stream)
+    if evpair:
+        evpair[0].record(stream)
     s.decode()
-    evpair[1].record(stream)
+    if evpair:
+        evpair[1].record(stream)
     if s.kind == "token":
         mla.project_out(s.cfg, s.o_lat, s.w_uv, s.o_v, s.w_o, s.out)
     else:

@@ -4,115 +4,209 @@
 // log-sum-exp lse_s.  The full result over the union of the ranges is
 //   LSE = log sum_s exp(lse_s),   o = sum_s exp(lse_s - LSE) * o_s,
 // which is exact because exp(lse_s) is the softmax denominator of range s.
-// Empty ranges carry lse = -inf and weigh nothing.  One CTA per (sequence,
-// head), threads over the latent width; HBM-bound, no tensor-core work.
+// Empty ranges carry lse = -inf and weigh nothing.
+//
+// One warp per (sequence, head), four heads per CTA: the lanes compute the
+// weights of up to 32 partials at a time with shuffles, then stream the
+// partial rows with 16-byte loads (HBM/L2-bound, no tensor-core work).  The
+// planned variant is launched as a programmatic dependent of the decode
+// kernel: its set-up overlaps the decode tail and it waits for the partials
+// with griddepcontrol.wait.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace mla {
 
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kMaxSlots = 1024;
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float a, float b, float c, float d) {
+    *(float4*)dst = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float a, float b,
+                                                      float c, float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    *(uint2*)dst = v;
+}
+
 template <typename T, bool kPlanned>
-__global__ void __launch_bounds__(128) combine_kernel(
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(
     const float* __restrict__ o_part, const float* __restrict__ lse_part, int n_splits,
     int batch, int heads, int DL, T* __restrict__ o_lat, float* __restrict__ lse,
-    const int32_t* __restrict__ seq_lens, int cap, int W) {
-    extern __shared__ int pre[];   // planned: [batch + 1]
-    __shared__ float wts[1024];
-    __shared__ int slots[1024];
+    const int32_t* __restrict__ seq_lens, int cap, int W, int tile) {
+    __shared__ int slots[kMaxSlots];
+    __shared__ float wts[kWarps][kMaxSlots];
+    __shared__ int red[2][kWarps];
     __shared__ int n_sl;
-    __shared__ float sh_lse;
-    const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y * kWarps + warp;
 
     if (kPlanned) {
-        tile_prefix(seq_lens, batch, cap, pre, nullptr);
+        pdl_wait();
+        // tiles of the sequences before b, and in all sequences
+        int before = 0, all = 0, mine = 0;
+        for (int j = tid; j < batch; j += blockDim.x) {
+            int n = seq_lens[j];
+            n = (n < 1) ? 0 : (n > cap ? cap : n);
+            const int t = (n + tile - 1) / tile;
+            all += t;
+            if (j < b) before += t;
+            if (j == b) mine = t;
+        }
+        before = __reduce_add_sync(0xffffffffu, before);
+        all = __reduce_add_sync(0xffffffffu, all);
+        mine = __reduce_add_sync(0xffffffffu, mine);
+        if (lane == 0) {
+            red[0][warp] = before;
+            red[1][warp] = all;
+        }
+        __shared__ int sh_mine[kWarps];
+        if (lane == 0) sh_mine[warp] = mine;
+        __syncthreads();
         if (tid == 0) {
-            const int64_t total = pre[batch];
+            int64_t p0 = 0, total = 0;
+            int t_b = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                p0 += red[0][w];
+                total += red[1][w];
+                t_b += sh_mine[w];
+            }
+            const int64_t p1 = p0 + t_b;
             int cnt = 0;
-            if (pre[b + 1] > pre[b]) {
-                // workers whose tile range meets [pre[b], pre[b+1])
-                int g = (int)((int64_t)pre[b] * W / total);
-                while (g > 0 && plan_lo(g, total, W) > pre[b]) --g;
-                while (g + 1 < W && plan_lo(g + 1, total, W) <= pre[b]) ++g;
-                for (; g < W && plan_lo(g, total, W) < pre[b + 1]; ++g) {
-                    if (plan_lo(g + 1, total, W) <= pre[b]) continue;
-                    if (plan_lo(g, total, W) >= plan_lo(g + 1, total, W)) continue;
-                    if (cnt < 1024) slots[cnt++] = g + b;
+            if (p1 > p0) {
+                // workers whose tile range [plan_lo(g), plan_lo(g+1)) meets [p0, p1)
+                int g = (int)(p0 * W / total);
+                while (g > 0 && plan_lo(g, total, W) > p0) --g;
+                while (g + 1 < W && plan_lo(g + 1, total, W) <= p0) ++g;
+                for (; g < W && plan_lo(g, total, W) < p1; ++g) {
+                    const int64_t glo = plan_lo(g, total, W), ghi = plan_lo(g + 1, total, W);
+                    if (ghi <= p0 || glo >= ghi) continue;
+                    if (cnt < kMaxSlots) slots[cnt++] = g + b;
                 }
             }
             n_sl = cnt;
         }
     } else {
-        if (tid == 0) {
-            int cnt = 0;
-            for (int s = 0; s < n_splits && cnt < 1024; ++s) slots[cnt++] = s;
-            n_sl = cnt;
-        }
+        for (int s = tid; s < n_splits && s < kMaxSlots; s += blockDim.x) slots[s] = s;
+        if (tid == 0) n_sl = n_splits < kMaxSlots ? n_splits : kMaxSlots;
     }
     __syncthreads();
+    if (h >= heads) return;
     const int ns = n_sl;
     auto lse_at = [&](int s) -> float {
         return kPlanned ? lse_part[(size_t)slots[s] * heads + h]
                         : lse_part[((size_t)slots[s] * batch + b) * heads + h];
     };
-    auto o_at = [&](int s) -> const float* {
+    auto row_at = [&](int s) -> const float* {
         return kPlanned ? o_part + ((size_t)slots[s] * heads + h) * DL
                         : o_part + (((size_t)slots[s] * batch + b) * heads + h) * DL;
     };
-    if (tid == 0) {
-        float m = -INFINITY;
-        for (int s = 0; s < ns; ++s) m = fmaxf(m, lse_at(s));
-        float sum = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            float l = lse_at(s);
-            float w = (l == -INFINITY) ? 0.f : expf(l - m);
-            wts[s] = w;
-            sum += w;
-        }
-        float inv = sum > 0.f ? 1.f / sum : 0.f;
-        for (int s = 0; s < ns; ++s) wts[s] *= inv;
-        sh_lse = sum > 0.f ? m + logf(sum) : -INFINITY;
+
+    // weights: max and sum over the slots, 32 at a time
+    float m = -INFINITY;
+    for (int s = lane; s < ns; s += 32) m = fmaxf(m, lse_at(s));
+    m = warp_max(m);
+    float sum = 0.f;
+    for (int s = lane; s < ns; s += 32) {
+        const float l = lse_at(s);
+        const float w = (l == -INFINITY) ? 0.f : expf(l - m);
+        wts[warp][s] = w;
+        sum += w;
     }
-    __syncthreads();
+    sum = warp_sum(sum);
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    __syncwarp();
+
     T* out = o_lat + ((size_t)b * heads + h) * DL;
-    for (int j = tid; j < DL; j += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            float w = wts[s];
-            if (w != 0.f) acc = fmaf(w, o_at(s)[j], acc);
+    if ((DL & 3) == 0) {
+        for (int j = lane * 4; j < DL; j += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            int s = 0;
+            for (; s + 1 < ns; s += 2) {
+                const float w0 = wts[warp][s] * inv, w1 = wts[warp][s + 1] * inv;
+                const float4 v0 = *(const float4*)(row_at(s) + j);
+                const float4 v1 = *(const float4*)(row_at(s + 1) + j);
+                if (w0 != 0.f) {
+                    acc.x = fmaf(w0, v0.x, acc.x); acc.y = fmaf(w0, v0.y, acc.y);
+                    acc.z = fmaf(w0, v0.z, acc.z); acc.w = fmaf(w0, v0.w, acc.w);
+                }
+                if (w1 != 0.f) {
+                    acc.x = fmaf(w1, v1.x, acc.x); acc.y = fmaf(w1, v1.y, acc.y);
+                    acc.z = fmaf(w1, v1.z, acc.z); acc.w = fmaf(w1, v1.w, acc.w);
+                }
+            }
+            if (s < ns) {
+                const float w0 = wts[warp][s] * inv;
+                const float4 v0 = *(const float4*)(row_at(s) + j);
+                if (w0 != 0.f) {
+                    acc.x = fmaf(w0, v0.x, acc.x); acc.y = fmaf(w0, v0.y, acc.y);
+                    acc.z = fmaf(w0, v0.z, acc.z); acc.w = fmaf(w0, v0.w, acc.w);
+                }
+            }
+            store4<T>(out + j, acc.x, acc.y, acc.z, acc.w);
         }
-        out[j] = from_f<T>(acc);
+    } else {
+        for (int j = lane; j < DL; j += 32) {
+            float acc = 0.f;
+            for (int s = 0; s < ns; ++s) {
+                const float w = wts[warp][s] * inv;
+                if (w != 0.f) acc = fmaf(w, row_at(s)[j], acc);
+            }
+            out[j] = from_f<T>(acc);
+        }
     }
-    if (lse && tid == 0) lse[(size_t)b * heads + h] = sh_lse;
+    if (lse && lane == 0) lse[(size_t)b * heads + h] = sum > 0.f ? m + logf(sum) : -INFINITY;
 }
 
+template <typename T, bool kPlanned>
+cudaError_t launch(const float* o_part, const float* lse_part, int n_splits, int batch,
+                   int heads, int DL, void* o_lat, float* lse, const int32_t* seq_lens, int cap,
+                   int W, int tile, bool pdl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(batch, (heads + kWarps - 1) / kWarps);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<T, kPlanned>, o_part, lse_part, n_splits,
+                              batch, heads, DL, (T*)o_lat, lse, seq_lens, cap, W, tile);
+}
+
+}  // namespace
+
 cudaError_t launch_combine_planned(const DecodeArgs& a, int dtype, cudaStream_t st) {
-    dim3 grid(a.batch, a.heads);
-    size_t sm = sizeof(int) * (size_t)(a.batch + 1);
-    int cap = a.max_blocks * a.block_size;
+    const int cap = a.max_blocks * a.block_size;
     if (dtype == MLA_DTYPE_BF16)
-        combine_kernel<__nv_bfloat16, true><<<grid, 128, sm, st>>>(
-            a.o_part, a.lse_part, 0, a.batch, a.heads, a.d_latent, (__nv_bfloat16*)a.o_lat,
-            a.lse, a.seq_lens, cap, a.workers);
-    else
-        combine_kernel<float, true><<<grid, 128, sm, st>>>(
-            a.o_part, a.lse_part, 0, a.batch, a.heads, a.d_latent, (float*)a.o_lat, a.lse,
-            a.seq_lens, cap, a.workers);
-    return cudaGetLastError();
+        return launch<__nv_bfloat16, true>(a.o_part, a.lse_part, 0, a.batch, a.heads,
+                                           a.d_latent, a.o_lat, a.lse, a.seq_lens, cap,
+                                           a.workers, a.tile, true, st);
+    return launch<float, true>(a.o_part, a.lse_part, 0, a.batch, a.heads, a.d_latent, a.o_lat,
+                               a.lse, a.seq_lens, cap, a.workers, a.tile, true, st);
 }
 
 cudaError_t launch_combine_dense(const float* o_part, const float* lse_part, int n_splits,
                                  int batch, int heads, int d_latent, void* o_lat, float* lse,
                                  int dtype, cudaStream_t st) {
-    dim3 grid(batch, heads);
+    if (n_splits > kMaxSlots) return cudaErrorInvalidValue;
     if (dtype == MLA_DTYPE_BF16)
-        combine_kernel<__nv_bfloat16, false><<<grid, 128, 0, st>>>(
-            o_part, lse_part, n_splits, batch, heads, d_latent, (__nv_bfloat16*)o_lat, lse,
-            nullptr, 0, 1);
-    else
-        combine_kernel<float, false><<<grid, 128, 0, st>>>(
-            o_part, lse_part, n_splits, batch, heads, d_latent, (float*)o_lat, lse, nullptr, 0,
-            1);
-    return cudaGetLastError();
+        return launch<__nv_bfloat16, false>(o_part, lse_part, n_splits, batch, heads, d_latent,
+                                            o_lat, lse, nullptr, 0, 1, 1, false, st);
+    return launch<float, false>(o_part, lse_part, n_splits, batch, heads, d_latent, o_lat, lse,
+                                nullptr, 0, 1, 1, false, st);
 }
 
 }  // namespace mla

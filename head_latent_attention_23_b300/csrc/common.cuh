@@ -47,8 +47,8 @@ __device__ __forceinline__ void flag(int* status, int code) {
 }
 
 // ---------------------------------------------------------------- split plan
-// The decode work is the sequence of 64-token tiles of all sequences laid end
-// to end.  Worker g of W takes the tile range [lo(g), lo(g+1)), which can
+// The decode work is the sequence of fixed-size token tiles (64 tokens on the
+// CUDA cores, 128 on the tensor cores) of all sequences laid end to end.  Worker g of W takes the tile range [lo(g), lo(g+1)), which can
 // cross sequence boundaries; each (worker, sequence) piece yields one partial
 // result in slot g + b.  Slots are unique (ranges are ordered) and fewer than
 // W + batch.
@@ -67,17 +67,23 @@ __device__ __forceinline__ int clamp_len(int n, int cap, int* status) {
     return n;
 }
 
-// Block-wide exclusive prefix of ceil(len_b / kTile) over b = 0..batch-1 into
-// pre[0..batch] (shared).  All threads must call.
+// Block-wide exclusive prefix of ceil(len_b / tile) over b = 0..batch-1 into
+// pre[0..batch] (shared); the clamped lengths go to lens[0..batch-1] when
+// lens is not null.  All threads must call.
 __device__ __forceinline__ void tile_prefix(const int32_t* seq_lens, int batch, int cap,
-                                            int* pre, int* status) {
+                                            int* pre, int* status, int* lens = nullptr,
+                                            int tile = kTile) {
     __shared__ int warp_tot[32];
     const int tid = threadIdx.x, nt = blockDim.x;
     int carry = 0;
     for (int base = 0; base < batch; base += nt) {
         int b = base + tid;
         int v = 0;
-        if (b < batch) v = (clamp_len(seq_lens[b], cap, status) + kTile - 1) / kTile;
+        if (b < batch) {
+            const int n = clamp_len(seq_lens[b], cap, status);
+            if (lens) lens[b] = n;
+            v = (n + tile - 1) / tile;
+        }
         // inclusive scan within the warp
         int lane = tid & 31, w = tid >> 5;
         int x = v;

@@ -7,27 +7,40 @@
 //   s_i = scale * (q_lat_h . c_i + q_pe_h . kr_i),  p = softmax(s),
 //   o_lat_h = sum_i p_i c_i
 // The 128 heads share every cache row, so S = Q C^T (M = 128 heads) and
-// O = P C are dense contractions and run on tcgen05 with TMEM accumulators.
+// O = P C are dense contractions; they run on tcgen05 with TMEM accumulators.
 //
-// Work split.  The 64-token tiles of all sequences, laid end to end, are cut
-// into W equal ranges; each range goes to a cluster of two CTAs.  CTA r of the
-// pair owns latent columns [256r, 256r+256) and rotary columns
-// [512+32r, 512+32r+32), so the pair reads each cache row exactly once:
-//   - TMA streams CTA r's 288 columns of each 64-token tile into a 5-stage
-//     ring (four 64x64 boxes, 128-byte swizzle, plus one 64x32 box, 64-byte
-//     swizzle);
-//   - one thread issues S_r = Q_r C_r^T (M=128, N=64, 18 k-steps, Q_r held in
-//     TMEM as the A operand) into TMEM;
-//   - the softmax warpgroup (thread = head) reads S_r, swaps it with the
-//     partner through distributed shared memory, and both CTAs form
-//     S = S_0 + S_1 in the same order, so they take bit-identical softmax
-//     decisions; the running max is only moved when a row's tile max exceeds
-//     it by more than 2^8 (rescaling O in TMEM is then rare and exact, since O
-//     and the row sum share the stale max); P (bf16) goes back into TMEM;
-//   - the same thread issues O_r += P C_r (M=128, N=256, 4 k-steps, C_r read
-//     N-major from the same smem stage), so O_r lives in 256 TMEM columns.
-// A range that ends a sequence writes the normalised partial o and its
-// log-sum-exp to slot g + b; the merge kernel combines the slots.
+// Layout across an SM pair.  O for 128 heads x 512 latent columns in fp32 is
+// 256 KB, all of one SM's tensor memory, and the absorbed query Q (128 x 576
+// bf16, 144 KB) is too large to sit next to any part of O.  A 2-CTA cluster
+// therefore splits the work by kind, not by columns:
+//   - the score CTA (rank 0) keeps the latent part of Q in TMEM (256 columns,
+//     brought in by TMA and tcgen05.cp at the start of each sequence's range;
+//     the rotary part sits in shared memory) and computes S = Q C^T for
+//     128-token tiles (M=128, N=128, K=576: 36 MMAs) into two alternating
+//     128-column TMEM buffers, so S(k) runs while S(k-1) is read; its softmax
+//     warps turn S into bf16 P, stage P in
+//     the operand layout of the next product and push it, 33 KB per tile,
+//     into the value CTA's shared memory with one bulk copy;
+//   - the value CTA (rank 1) keeps O in all 512 TMEM columns and computes
+//     O += P C (M=128, N=256, K=128: 16 MMAs) from its own copy of the tile's
+//     latent columns.
+// Each CTA streams what it needs with TMA (128-byte swizzle): the score CTA
+// takes all 576 columns of a tile in nine 64-column chunks of 128 tokens (two
+// 64-row boxes each, since the two pages of a tile need not be adjacent), the
+// value CTA takes the 512 latent columns in four (column half, page) chunks,
+// each one box of 64 rows x four 64-column groups of a 3-D view of the cache,
+// which hit L2 right after the score CTA brought them in.  Only P crosses the
+// cluster; distributed shared memory moves about 12 bytes per clock, so the
+// fp32 partial scores of a column split (64 KB per tile each way) would not fit.
+//
+// Softmax.  Thread h of the score CTA owns head h (TMEM lane h).  The running
+// max m only moves when a tile's max exceeds it by more than 2^8; the tile's
+// message then carries the factor 2^(m_old - m_new) per head and the value
+// CTA rescales its O rows before adding the tile (rare, and exact because O
+// and the row sum share the stale max).  The row sum uses the bf16-rounded
+// weights the product sees.  The last tile of a sequence's range also carries
+// 1 / sum, so the value CTA writes the normalised partial o and the score CTA
+// its log-sum-exp (slot g + b); the merge kernel combines the slots.
 //
 // Every wait is bounded (see tc_ptx.cuh); on a timeout the kernel records
 // MLA_ERR_TIMEOUT, lets its copies land, frees TMEM and returns.
@@ -42,34 +55,70 @@ namespace {
 using namespace tc;
 
 constexpr int kHeads = 128, kDL = 512, kDR = 64, kD = kDL + kDR;
-constexpr int kT = 64;                 // tokens per tile
-constexpr int kStages = 5;
-constexpr int kLatBox = kT * 64 * 2;   // 8 KB: 64 tokens x 64 latent columns
-constexpr int kRopeBox = kT * 32 * 2;  // 4 KB: 64 tokens x 32 rotary columns
-constexpr int kStageBytes = 4 * kLatBox + kRopeBox;   // 36 KB
-constexpr int kXBytes = kHeads * kT * 4;               // 32 KB partial-score swap
+constexpr int kT = 128;                  // tokens per tile
+constexpr int kHalf = 64;                // rows per TMA box (a tile = two boxes)
+constexpr int kBox = kHalf * 64 * 2;     // 8 KB: 64 rows x 64 columns
+// score CTA ring: 64 columns x 128 tokens per chunk, nine chunks per tile
+constexpr int kSChunk = 2 * kBox;
+constexpr int kSChunks = 9;
+constexpr int kSSlots = 8;
+// value CTA ring: 256 columns x 64 tokens per chunk, four chunks per tile
+constexpr int kVChunk = 4 * kBox;
+constexpr int kVChunks = 4;
+constexpr int kVSlots = 4;
+constexpr int kRingBytes = kSSlots * kSChunk;
+static_assert(kRingBytes == kVSlots * kVChunk, "one ring region for both roles");
+// message: P [128 heads x 128 tokens] bf16 as two K-major 128-byte-swizzled
+// blocks of 64 tokens, then the per-head factors
+constexpr int kPBytes = kHeads * kT * 2;   // 32 KB
+constexpr int kAuxBytes = 2048;    // factors, row sums, flags, valid rows
+constexpr int kMsgBytes = kPBytes + kAuxBytes;
+constexpr int kMsgSlots = 2;             // value CTA: two receive slots
+constexpr int kQChunks = 8;              // latent query: eight 128-head x 64-column chunks
+constexpr int kQpeBytes = kHeads * kDR * 2;   // 16 KB
 constexpr int kMaxBatch = 1024;
-constexpr int kBarOff = kStages * kStageBytes + kXBytes;
-constexpr int kPreOff = kBarOff + 256;
-constexpr int kSmemBytes = 1024 + kPreOff + (kMaxBatch + 1) * 4;
-constexpr int kThreads = 192;
+// The score CTA stages one outgoing message at kMsgOff and keeps the rotary
+// query of two consecutive ranges in the space of the second receive slot.
+constexpr int kMsgOff = kRingBytes;
+constexpr int kQpeOff = kMsgOff + kMsgBytes;
+static_assert(2 * kQpeBytes <= kMsgBytes, "rotary query buffers");
+constexpr int kBarOff = kMsgOff + kMsgSlots * kMsgBytes;
+constexpr int kRedOff = kBarOff + 512;     // softmax exchange: [4][128] fp32
+constexpr int kPreOff = kRedOff + 4 * 128 * 4;
+constexpr int kLenOff = kPreOff + (kMaxBatch + 1) * 4;
+constexpr int kSmemBytes = 1024 + kLenOff + kMaxBatch * 4;
+constexpr int kThreads = 320;      // producer, MMA, 8 softmax / epilogue warps
+static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kMsgBytes % 1024 == 0, "message slots keep the 1 KB swizzle alignment");
+
+// aux block of a message (offsets in 4-byte words after P)
+constexpr int kAuxAlpha = 0;     // [128] factor applied to O rows before this tile
+constexpr int kAuxSum = 128;     // [2][128] row sums of the two token halves (last tile)
+constexpr int kAuxFlags = 384;   // [4] per softmax warp: some row of it rescales
+constexpr int kAuxValid = 388;   // [2] valid rows of the two 64-token halves
+static_assert((kAuxValid + 2) * 4 <= kAuxBytes, "aux block");
 
 // TMEM columns
-constexpr uint32_t kColO = 0;      // 256: O_r, fp32 [head][latent col]
-constexpr uint32_t kColQ = 256;    // 144: Q_r, bf16 pairs [head][k]
-constexpr uint32_t kColS = 400;    // 64:  S_r, fp32 [head][token]
-constexpr uint32_t kColP = 464;    // 32:  P, bf16 pairs [head][token]
+constexpr uint32_t kColQ = 0;      // score CTA: 256 columns, latent Q bf16 pairs [head][k]
+constexpr uint32_t kColS = 256;    // score CTA: 2 x 128 columns, S fp32 [head][token]
+constexpr uint32_t kColO = 0;      // value CTA: 512 columns, O fp32 [head][latent]
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 struct Bars {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t s_full, s_empty, p_full, p_empty, q_ready, o_free, x_full, x_empty, mma_done;
+    uint64_t cfull[8], cempty[8];           // chunk ring
+    uint64_t s_full[2], s_empty[2];         // score CTA: S double buffer
+    uint64_t qpe_full[2], qpe_free[2];      // score CTA: rotary query of a range
+    uint64_t p_empty[kMsgSlots];            // score CTA: value CTA freed a message slot
+    uint64_t p_full[kMsgSlots];             // value CTA: message landed
+    uint64_t pv_done[kMsgSlots];            // value CTA: PV of the slot's tile finished
+    uint64_t zeroed, resc_done, o_free, mma_done;
+    uint64_t wg;                            // softmax-warpgroup rendezvous
     uint32_t tmem_slot;
     int abort_flag;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // Walks the tiles of one worker range in order.
 struct Cursor {
@@ -93,48 +142,116 @@ struct Cursor {
     __device__ bool last(int64_t hi) const { return t + 1 == hi || t + 1 == pre[b + 1]; }
 };
 
+// Cache rows of the two 64-token halves of tile `t0` (first token) of
+// sequence b with n tokens, and how many of each half's rows are real.
+// Halves past the sequence end or on an invalid page read row 0 (always in
+// the pool) and count zero valid rows.
+struct TileRows {
+    int row[2];
+    int valid[2];
+};
+__device__ __forceinline__ TileRows tile_rows(const DecodeArgs& a, int b, int n, int t0,
+                                              bool report) {
+    TileRows r;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int tok = t0 + half * kHalf;
+        r.row[half] = 0;
+        r.valid[half] = 0;
+        if (tok < n) {
+            const int32_t blk = a.block_table[(size_t)b * a.max_blocks + tok / a.block_size];
+            if (blk >= 0 && blk < a.num_blocks) {
+                r.row[half] = blk * a.block_size + tok % a.block_size;
+                r.valid[half] = min(kHalf, n - tok);
+            } else if (report) {
+                flag(a.status, MLA_ERR_INDEX);
+            }
+        }
+    }
+    return r;
+}
+
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                         uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most N bulk groups of this thread still read their source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap t_lat,
-                     const __grid_constant__ CUtensorMap t_rope, const DecodeArgs a) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap t_cache,
+                     const __grid_constant__ CUtensorMap t_cache2,
+                     const __grid_constant__ CUtensorMap t_page,
+                     const __grid_constant__ CUtensorMap t_qlat,
+                     const __grid_constant__ CUtensorMap t_qpe,
+                     const __grid_constant__ DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float* X = (float*)(smem + kStages * kStageBytes);
+    uint8_t* ring = smem;
+    uint8_t* msg = smem + kMsgOff;
     Bars* bars = (Bars*)(smem + kBarOff);
     int* pre = (int*)(smem + kPreOff);
+    int* lens = (int*)(smem + kLenOff);
     volatile int* abort_flag = &bars->abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const uint32_t peer = rank ^ 1u;
+    const bool scorer = rank == 0;
     const int g = blockIdx.x >> 1;
     const int cap = a.max_blocks * a.block_size;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], 1);
+        for (int s = 0; s < 8; ++s) {
+            mbar_init(&bars->cfull[s], 1);
+            mbar_init(&bars->cempty[s], 1);
         }
-        mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->s_empty, 128);
-        mbar_init(&bars->p_full, 128);
-        mbar_init(&bars->p_empty, 1);
-        mbar_init(&bars->q_ready, 128);
-        mbar_init(&bars->o_free, 128);
-        mbar_init(&bars->x_full, 128);
-        mbar_init(&bars->x_empty, 128);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->s_empty[s], 256);
+            mbar_init(&bars->qpe_full[s], 1);
+            mbar_init(&bars->qpe_free[s], 1);
+        }
+        for (int s = 0; s < kMsgSlots; ++s) {
+            mbar_init(&bars->p_empty[s], 8);     // one remote arrive per value-CTA warp
+            mbar_init(&bars->p_full[s], 1);      // local expect_tx + the bulk copy
+            mbar_init(&bars->pv_done[s], 1);
+        }
+        mbar_init(&bars->zeroed, 256);
+        mbar_init(&bars->resc_done, 256);
+        mbar_init(&bars->o_free, 256);
         mbar_init(&bars->mma_done, 1);
+        mbar_init(&bars->wg, 256);
         bars->abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&t_lat);
-        prefetch_tmap(&t_rope);
+        prefetch_tmap(&t_cache);
+        prefetch_tmap(&t_cache2);
+        prefetch_tmap(&t_page);
+        prefetch_tmap(&t_qlat);
+        prefetch_tmap(&t_qpe);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    tile_prefix(a.seq_lens, a.batch, cap, pre, a.status);   // ends with __syncthreads
+    // everything above overlaps the previous kernel's tail; inputs are read
+    // only once it has finished
+    pdl_wait_primary();
+    tile_prefix(a.seq_lens, a.batch, cap, pre, scorer ? a.status : nullptr, lens, kT);
     tc_fence_before();
-    cluster_sync();        // both CTAs' barriers exist before any remote arrive
+    cluster_sync();        // both CTAs' barriers exist before any remote access
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
 
@@ -147,277 +264,456 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0 && K > 0) {
             Cursor cur;
             cur.init(pre, a.batch, lo);
-            int issued = 0;
-            for (int k = 0; k < K; ++k, cur.next()) {
-                const int s = k % kStages;
-                if (!mbar_wait(&bars->empty[s], ((k / kStages) & 1) ^ 1, abort_flag, a.status))
-                    break;
-                const int tok = cur.tile_in_seq() * kT;
-                int32_t blk = a.block_table[(size_t)cur.b * a.max_blocks + tok / a.block_size];
-                if (blk < 0 || blk >= a.num_blocks) {
-                    flag(a.status, MLA_ERR_INDEX);
-                    blk = 0;   // load a valid page; the softmax masks the whole tile
+            int c = 0, seg = 0;
+            bool ok = true;
+            auto ring_slot = [&](int slots, int bytes) -> int {
+                const int s = c % slots;
+                if (!mbar_wait_fast(&bars->cempty[s], ((c / slots) & 1) ^ 1, abort_flag,
+                                    a.status)) {
+                    ok = false;
+                    return -1;
                 }
-                const int y = blk * a.block_size + tok % a.block_size;
-                uint8_t* st = smem + s * kStageBytes;
-                mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    tma_load_2d(st + i * kLatBox, &t_lat, 256 * rank + 64 * i, y, &bars->full[s]);
-                tma_load_2d(st + 4 * kLatBox, &t_rope, kDL + 32 * rank, y, &bars->full[s]);
-                issued = k + 1;
+                mbar_arrive_expect_tx(&bars->cfull[s], bytes);
+                return s;
+            };
+            for (int k = 0; k < K && ok; ++k, cur.next()) {
+                const int t0 = cur.tile_in_seq() * kT;
+                const TileRows tr = tile_rows(a, cur.b, lens[cur.b], t0, scorer);
+                if (scorer) {
+                    if (cur.first(lo)) {
+                        // the range's query: the rotary part into its own buffer
+                        // (free once the previous use's products are done), the
+                        // latent part through the ring for tcgen05.cp into TMEM
+                        const int qb = seg & 1;
+                        if (!mbar_wait_fast(&bars->qpe_free[qb], ((seg >> 1) & 1) ^ 1,
+                                            abort_flag, a.status))
+                            break;
+                        mbar_arrive_expect_tx(&bars->qpe_full[qb], kQpeBytes);
+                        tma_load_2d(smem + kQpeOff + qb * kQpeBytes, &t_qpe, 0, cur.b * kHeads,
+                                    &bars->qpe_full[qb]);
+                        ++seg;
+                        for (int j = 0; j < kQChunks && ok; ++j, ++c) {
+                            const int s = ring_slot(kSSlots, kSChunk);
+                            if (s < 0) break;
+                            tma_load_2d(ring + s * kSChunk, &t_qlat, 64 * j, cur.b * kHeads,
+                                        &bars->cfull[s]);
+                        }
+                        if (!ok) break;
+                    }
+                    // the two pages of the tile in one 128-row box when they are
+                    // adjacent in the pool (fewer, larger TMA requests), else one
+                    // 64-row box each; the shared-memory image is the same
+                    const bool adjacent = tr.valid[1] > 0 && tr.row[1] == tr.row[0] + kHalf;
+                    for (int j = 0; j < kSChunks && ok; ++j, ++c) {
+                        const int s = ring_slot(kSSlots, kSChunk);
+                        if (s < 0) break;
+                        uint8_t* dst = ring + s * kSChunk;
+                        if (adjacent) {
+                            tma_load_2d(dst, &t_cache2, 64 * j, tr.row[0], &bars->cfull[s]);
+                        } else {
+                            tma_load_2d(dst, &t_cache, 64 * j, tr.row[0], &bars->cfull[s]);
+                            tma_load_2d(dst + kBox, &t_cache, 64 * j, tr.row[1], &bars->cfull[s]);
+                        }
+                    }
+                } else {
+                    // one box per chunk: 64 rows of a page x four 64-column groups
+                    for (int j = 0; j < kVChunks && ok; ++j, ++c) {
+                        const int s = ring_slot(kVSlots, kVChunk);
+                        if (s < 0) break;
+                        tma_load_3d(ring + s * kVChunk, &t_page, 0, tr.row[j & 1], 4 * (j >> 1),
+                                    &bars->cfull[s]);
+                    }
+                }
             }
-            for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
-                drain_wait(&bars->full[k % kStages], (k / kStages) & 1);
+            // every copy this thread started has landed before the CTA exits
+            const int slots = scorer ? kSSlots : kVSlots;
+            for (int i = c > slots ? c - slots : 0; i < c; ++i)
+                drain_wait(&bars->cfull[i % slots], (i / slots) & 1);
+            if (scorer)
+                for (int i = seg > 2 ? seg - 2 : 0; i < seg; ++i)
+                    drain_wait(&bars->qpe_full[i & 1], (i >> 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0 && K > 0) {
-            const uint32_t id_s = idesc_bf16(128, kT, false, false);
-            const uint32_t id_pv = idesc_bf16(128, 256, false, true);
-            Cursor cur, pvc;
+            Cursor cur;
             cur.init(pre, a.batch, lo);
-            pvc.init(pre, a.batch, lo);
-            int seg = 0, pv_seg = 0;
             bool ok = true;
-            auto issue_pv = [&](int k) -> bool {
-                const int s = k % kStages;
-                const bool first = pvc.first(lo);
-                if (first && pv_seg > 0 &&
-                    !mbar_wait(&bars->o_free, (pv_seg - 1) & 1, abort_flag, a.status))
-                    return false;
-                if (!mbar_wait(&bars->p_full, k & 1, abort_flag, a.status)) return false;
-                tc_fence_after();
-                const uint32_t st = smem_u32(smem + s * kStageBytes);
+            if (scorer) {
+                // S = Q C^T, K = 576 in nine 64-column chunks of four k-steps
+                const uint32_t id_s = idesc_bf16(128, kT, false, false);
+                int c = 0, seg = 0, qb = 0;
+                for (int k = 0; k < K && ok; ++k, cur.next()) {
+                    if (cur.first(lo)) {
+                        // new range: its latent query chunks into TMEM (in order
+                        // after the previous range's products), then its rotary part
+                        for (int j = 0; j < kQChunks; ++j, ++c) {
+                            const int s = c % kSSlots;
+                            if (!mbar_wait_fast(&bars->cfull[s], (c / kSSlots) & 1, abort_flag,
+                                                a.status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t st = smem_u32(ring + s * kSChunk);
 #pragma unroll
-                for (int i = 0; i < kT / 16; ++i) {
-                    const uint64_t bd = sdesc(st + 2048 * i, kLatBox, 1024, 2);
-                    mma_ts(tmem + kColO, tmem + kColP + 8 * i, bd, id_pv,
-                           (first && i == 0) ? 0 : 1);
-                }
-                tc_commit(&bars->empty[s]);
-                tc_commit(&bars->p_empty);
-                if (pvc.last(hi)) ++pv_seg;
-                pvc.next();
-                return true;
-            };
-            for (int k = 0; k < K && ok; ++k, cur.next()) {
-                const int s = k % kStages;
-                if (cur.first(lo) && !mbar_wait(&bars->q_ready, seg & 1, abort_flag, a.status))
-                    break;
-                if (!mbar_wait(&bars->full[s], (k / kStages) & 1, abort_flag, a.status)) break;
-                if (!mbar_wait(&bars->s_empty, (k & 1) ^ 1, abort_flag, a.status)) break;
-                tc_fence_after();
-                const uint32_t st = smem_u32(smem + s * kStageBytes);
+                            for (int kk = 0; kk < 4; ++kk)
+                                tmem_cp_128x256b(tmem + kColQ + 32 * j + 8 * kk,
+                                                 sdesc(st + 32 * kk, 16, 1024, 2));
+                            tc_commit(&bars->cempty[s]);
+                        }
+                        if (!ok) break;
+                        qb = seg & 1;
+                        if (!mbar_wait_fast(&bars->qpe_full[qb], (seg >> 1) & 1, abort_flag,
+                                            a.status))
+                            break;
+                        ++seg;
+                    }
+                    const int sb = k & 1;   // S buffer: the softmax warps read S(k-1) meanwhile
+                    if (!mbar_wait_fast(&bars->s_empty[sb], ((k >> 1) & 1) ^ 1, abort_flag,
+                                        a.status))
+                        break;
+                    tc_fence_after();
+                    const uint32_t d_s = tmem + kColS + 128 * sb;
+                    const uint32_t qa = smem_u32(smem + kQpeOff + qb * kQpeBytes);
+                    for (int j = 0; j < kSChunks; ++j, ++c) {
+                        const int s = c % kSSlots;
+                        if (!mbar_wait_fast(&bars->cfull[s], (c / kSSlots) & 1, abort_flag,
+                                            a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = smem_u32(ring + s * kSChunk);
+                        if (j < kSChunks - 1) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint64_t bd = sdesc(st + (i >> 2) * kLatBox + 32 * (i & 3), 16, 1024, 2);
-                    mma_ts(tmem + kColS, tmem + kColQ + 8 * i, bd, id_s, i > 0);
-                }
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ts(d_s, tmem + kColQ + 32 * j + 8 * kk,
+                                       sdesc(st + 32 * kk, 16, 1024, 2), id_s, (j | kk) != 0);
+                        } else {
+                            // rotary part: Q_pe from shared memory
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const uint64_t bd = sdesc(st + 4 * kLatBox + 32 * i, 16, 512, 4);
-                    mma_ts(tmem + kColS, tmem + kColQ + 128 + 8 * i, bd, id_s, 1);
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(d_s, sdesc(qa + 32 * kk, 16, 1024, 2),
+                                       sdesc(st + 32 * kk, 16, 1024, 2), id_s, 1);
+                        }
+                        tc_commit(&bars->cempty[s]);
+                    }
+                    if (!ok) break;
+                    tc_commit(&bars->s_full[sb]);
+                    if (cur.last(hi)) tc_commit(&bars->qpe_free[qb]);
                 }
-                tc_commit(&bars->s_full);
-                if (k > 0) ok = issue_pv(k - 1);
-                if (cur.last(hi)) ++seg;
-                if (ok && k == K - 1) ok = issue_pv(k);
+            } else {
+                // O += P C, per column half: K = 128 tokens = two 64-token chunks
+                const uint32_t id_pv = idesc_bf16(128, 256, false, true);
+                int c = 0, seg = 0, resc = 0, zer = 0;
+                for (int k = 0; k < K && ok; ++k, cur.next()) {
+                    const int slot = k % kMsgSlots;
+                    const bool first = cur.first(lo);
+                    mbar_arrive_expect_tx(&bars->p_full[slot], kMsgBytes);
+                    if (!mbar_wait_fast<true>(&bars->p_full[slot], (k / kMsgSlots) & 1,
+                                              abort_flag, a.status))
+                        break;
+                    const uint8_t* m = msg + slot * kMsgBytes;
+                    const int* aux = (const int*)(m + kPBytes);
+                    const bool need_resc =
+                        !first && (aux[kAuxFlags] | aux[kAuxFlags + 1] | aux[kAuxFlags + 2] |
+                                   aux[kAuxFlags + 3]) != 0;
+                    const bool partial = aux[kAuxValid] < kHalf || aux[kAuxValid + 1] < kHalf;
+                    if (first && seg > 0 &&
+                        !mbar_wait_fast(&bars->o_free, (seg - 1) & 1, abort_flag, a.status))
+                        break;
+                    if (need_resc &&
+                        !mbar_wait_fast(&bars->resc_done, (resc++) & 1, abort_flag, a.status))
+                        break;
+                    if (partial &&
+                        !mbar_wait_fast(&bars->zeroed, (zer++) & 1, abort_flag, a.status))
+                        break;
+                    tc_fence_after();
+                    const uint32_t pa = smem_u32(m);
+                    for (int j = 0; j < kVChunks; ++j, ++c) {
+                        const int s = c % kVSlots, hh = j >> 1, pg = j & 1;
+                        if (!mbar_wait_fast(&bars->cfull[s], (c / kVSlots) & 1, abort_flag,
+                                            a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = smem_u32(ring + s * kVChunk);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            mma_ss(tmem + kColO + 256 * hh,
+                                   sdesc(pa + pg * (kPBytes / 2) + 32 * i, 16, 1024, 2),
+                                   sdesc(st + 2048 * i, kBox, 1024, 2), id_pv,
+                                   (first && pg == 0 && i == 0) ? 0 : 1);
+                        tc_commit(&bars->cempty[s]);
+                    }
+                    if (!ok) break;
+                    tc_commit(&bars->pv_done[slot]);
+                    if (cur.last(hi)) ++seg;
+                }
             }
             tc_commit(&bars->mma_done);
             drain_wait(&bars->mma_done, 0);
         }
-    } else {
-        // ------------------------------------------------ softmax warpgroup
+    } else if (K > 0) {
+        // warps 2-9: two threads per head.  TMEM lanes are reachable from the
+        // warps with the same (warp % 4), so warps w and w+4 share head
+        // h = 32 (w % 4) + lane; `half` picks 64 of the tile's 128 tokens (score
+        // CTA) or 256 of the 512 latent columns (value CTA).
         const int q4 = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int h = q4 * 32 + lane;                 // head = TMEM lane
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const int tid = threadIdx.x - 64;             // 0..127
-        const float c2 = a.scale * 1.4426950408889634f;
-        const uint32_t x_local = smem_u32(X);
-        const uint32_t x_peer = mapa(x_local, peer);
-        const uint32_t xfull_peer = mapa(smem_u32(&bars->x_full), peer);
-        const uint32_t xempty_peer = mapa(smem_u32(&bars->x_empty), peer);
-        const __nv_bfloat16* qlat = (const __nv_bfloat16*)a.q_lat;
-        const __nv_bfloat16* qpe = (const __nv_bfloat16*)a.q_pe;
+        const int tid = threadIdx.x - 64;             // 0..255
+        Cursor cur;
+        cur.init(pre, a.batch, lo);
+        if (scorer) {
+            // ------------------------------------------ softmax warpgroup
+            const float c2 = a.scale * 1.4426950408889634f;   // log2(e) / sqrt(d)
+            const uint32_t msg_peer = mapa(smem_u32(msg), 1);
+            const uint32_t pfull_peer = mapa(smem_u32(&bars->p_full[0]), 1);
+            float* red = (float*)(smem + kRedOff);     // [2][128] per-half tile max
 
-        auto load_q = [&](int b) {
-            const uint4* src = (const uint4*)(qlat + ((size_t)b * kHeads + h) * kDL + 256 * rank);
-#pragma unroll 4
-            for (int c = 0; c < 16; ++c) {
-                uint4 v0 = src[2 * c], v1 = src[2 * c + 1];
-                uint32_t r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                MLA_TMEM_ST_X8(tmem + lane_off + kColQ + 8 * c, r);
-            }
-            const uint4* sp = (const uint4*)(qpe + ((size_t)b * kHeads + h) * kDR + 32 * rank);
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint4 v0 = sp[2 * c], v1 = sp[2 * c + 1];
-                uint32_t r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                MLA_TMEM_ST_X8(tmem + lane_off + kColQ + 128 + 8 * c, r);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bars->q_ready);
-        };
+            // rendezvous of the 256 softmax threads: an mbarrier with a bounded
+            // wait, so a timeout anywhere releases everyone
+            uint32_t wg_phase = 0;
+            auto wg_sync = [&]() -> bool {
+                mbar_arrive(&bars->wg);
+                return mbar_wait_fast(&bars->wg, (wg_phase++) & 1, abort_flag, a.status);
+            };
 
-        if (K > 0) {
-            Cursor cur;
-            cur.init(pre, a.batch, lo);
-            load_q(cur.b);
-            float m = -INFINITY, l = 0.f;
+            float m = -INFINITY, l = 0.f;     // m: running max (log2 units); l: this half's sum
             for (int k = 0; k < K; ++k, cur.next()) {
-                const bool first = cur.first(lo), last = cur.last(hi);
                 const int b = cur.b;
-                const int n = clamp_len(a.seq_lens[b], cap, nullptr);
-                const int tok = cur.tile_in_seq() * kT;
-                int n_valid = min(kT, n - tok);
-                const int32_t blk = a.block_table[(size_t)b * a.max_blocks + tok / a.block_size];
-                if (blk < 0 || blk >= a.num_blocks) n_valid = 0;
+                const bool first = cur.first(lo), last = cur.last(hi);
+                const TileRows tr = tile_rows(a, b, lens[b], cur.tile_in_seq() * kT, false);
+                const int nv = tr.valid[half];          // valid tokens of this thread's 64
+                const int buf = k % kMsgSlots;
 
-                // ---- partial scores S_r
-                if (!mbar_wait(&bars->s_full, k & 1, abort_flag, a.status)) break;
+                // ---- this thread's 64 scores
+                const int sb = k & 1;
+                if (!mbar_wait_fast(&bars->s_full[sb], (k >> 1) & 1, abort_flag, a.status))
+                    break;
                 tc_fence_after();
-                float sv[kT];
+                float sv[kHalf];
                 {
-                    uint32_t r[16];
+                    const uint32_t src = tmem + lane_off + kColS + 128 * sb + 64 * half;
+                    uint32_t r[64];
+                    MLA_TMEM_LD_X32(src, r);
+                    MLA_TMEM_LD_X32(src + 32, (r + 32));
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < kT; c += 16) {
-                        MLA_TMEM_LD_X16(tmem + lane_off + kColS + c, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) sv[c + i] = __uint_as_float(r[i]);
-                    }
+                    for (int i = 0; i < kHalf; ++i) sv[i] = __uint_as_float(r[i]);
                 }
                 tc_fence_before();
-                mbar_arrive(&bars->s_empty);
+                mbar_arrive(&bars->s_empty[sb]);
 
-                // ---- swap partial scores with the peer CTA
-                if (!mbar_wait<true>(&bars->x_empty, (k & 1) ^ 1, abort_flag, a.status)) break;
+                // ---- tile max of the raw scores (the scale is positive)
+                float mx[8];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int pc = c ^ (h & 7);
-                    st_cluster_v4(x_peer + (uint32_t)((h * kT + 4 * pc) * 4), sv[4 * c],
-                                  sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
-                }
-                mbar_arrive_remote(xfull_peer);
-                if (!mbar_wait<true>(&bars->x_full, k & 1, abort_flag, a.status)) break;
+                for (int j = 0; j < 8; ++j) mx[j] = -INFINITY;
+                if (nv == kHalf) {
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int pc = c ^ (h & 7);
-                    const float4 o = *(const float4*)(X + h * kT + 4 * pc);
-                    // S = S_0 + S_1 in this order on both CTAs
-                    if (rank == 0) {
-                        sv[4 * c] += o.x; sv[4 * c + 1] += o.y;
-                        sv[4 * c + 2] += o.z; sv[4 * c + 3] += o.w;
-                    } else {
-                        sv[4 * c] = o.x + sv[4 * c]; sv[4 * c + 1] = o.y + sv[4 * c + 1];
-                        sv[4 * c + 2] = o.z + sv[4 * c + 2]; sv[4 * c + 3] = o.w + sv[4 * c + 3];
+                    for (int i = 0; i < kHalf; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kHalf; ++i) {
+                        if (i >= nv) sv[i] = -INFINITY;
+                        mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
                     }
                 }
-                mbar_arrive_remote(xempty_peer);
+                float mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                // the staging buffer is free once the copy of tile k-1 read it
+                if (tid == 0) bulk_wait_read<0>();
+                red[half * kHeads + h] = mloc;
+                if (!wg_sync()) break;
+                const float mt = fmaxf(mloc, red[(half ^ 1) * kHeads + h]) * c2;
 
-                // the next segment's query may replace Q now: S(k) is done
-                if (last && k + 1 < K) {
-                    Cursor nx = cur;
-                    nx.next();
-                    load_q(nx.b);
-                }
-
-                // ---- online softmax (log2 domain), lazy rescale
-                float mt = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < kT; ++i) {
-                    const float v = (i < n_valid) ? sv[i] * c2 : -INFINITY;
-                    sv[i] = v;
-                    mt = fmaxf(mt, v);
-                }
+                // ---- online softmax (log2 domain), lazy rescale; both threads
+                // of a head take the same decisions from the same values
                 const bool grow = mt > m + kRescaleThreshold;
                 float alpha = 1.f;
                 if (grow) {
-                    alpha = exp2f(m - mt);    // 0 when m = -inf
+                    alpha = ex2(m - mt);    // 0 when m = -inf
                     l *= alpha;
                     m = mt;
                 }
-                if (!first && __any_sync(0xffffffffu, grow)) {
-                    // O must hold every earlier PV of this segment: PV(k-1) done
-                    if (!mbar_wait(&bars->p_empty, (k - 1) & 1, abort_flag, a.status)) break;
-                    tc_fence_after();
-                    uint32_t r[16];
-                    for (int c = 0; c < 256; c += 16) {
-                        MLA_TMEM_LD_X16(tmem + lane_off + kColO + c, r);
-                        tmem_ld_wait();
+                const bool resc = grow && !first;
+
+                // ---- P: bf16 weights, 8 tokens = one 16-byte chunk at a time,
+                // in the 128-byte-swizzled K-major layout of the PV operand
+                uint8_t* mb = msg;     // the one staging buffer
+                uint8_t* row = mb + half * (kPBytes / 2) + h * 128;
+                const float nm = m == -INFINITY ? 0.f : -m;   // all-masked tile: p = 0
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        MLA_TMEM_ST_X16(tmem + lane_off + kColO + c, r);
-                    }
-                    tmem_st_wait();
-                }
-                uint32_t pk[kT / 2];
-                float ps = 0.f;
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t w[4];
 #pragma unroll
-                for (int i = 0; i < kT; i += 2) {
-                    const float p0 = (sv[i] == -INFINITY) ? 0.f : exp2f(sv[i] - m);
-                    const float p1 = (sv[i + 1] == -INFINITY) ? 0.f : exp2f(sv[i + 1] - m);
-                    ps += p0 + p1;
-                    pk[i / 2] = pack_bf16(p0, p1);
-                }
-                l += ps;
-
-                // ---- rows past the sequence end hold arbitrary bytes: zero
-                // them so 0 * garbage cannot reach O
-                if (n_valid < kT) {
-                    uint8_t* st = smem + (k % kStages) * kStageBytes;
-                    const int rows = kT - n_valid;
-                    for (int e = tid; e < rows * 4 * 8; e += 128) {
-                        const int box = e / (rows * 8), rem = e % (rows * 8);
-                        const int row = n_valid + rem / 8, ch = rem % 8;
-                        *(uint4*)(st + box * kLatBox + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < 4; ++i) {
+                        const float v0 = sv[8 * cc + 2 * i], v1 = sv[8 * cc + 2 * i + 1];
+                        // masked scores are -inf and give exp2(-inf) = 0
+                        const float p0 = ex2(fmaf(v0, c2, nm));
+                        const float p1 = ex2(fmaf(v1, c2, nm));
+                        ps[i] += p0 + p1;
+                        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                        w[i] = *reinterpret_cast<const uint32_t*>(&pb);
                     }
-                    fence_proxy_async();
+                    *(uint4*)(row + ((cc ^ (h & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
+                l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
 
-                // ---- P into TMEM once PV(k-1) has read the previous P
-                if (!mbar_wait(&bars->p_empty, (k & 1) ^ 1, abort_flag, a.status)) break;
-                tc_fence_after();
-                MLA_TMEM_ST_X16(tmem + lane_off + kColP, pk);
-                MLA_TMEM_ST_X16(tmem + lane_off + kColP + 16, (pk + 16));
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(&bars->p_full);
-
+                float* aux = (float*)(mb + kPBytes);
+                if (half == 0) {
+                    aux[kAuxAlpha + h] = resc ? alpha : 1.f;
+                    const bool any = __any_sync(0xffffffffu, resc);
+                    if (lane == 0) ((int*)aux)[kAuxFlags + q4] = any ? 1 : 0;
+                }
+                if (last) aux[kAuxSum + half * kHeads + h] = l;
+                if (tid == 0) {
+                    ((int*)aux)[kAuxValid] = tr.valid[0];
+                    ((int*)aux)[kAuxValid + 1] = tr.valid[1];
+                }
+                fence_proxy_async();
+                if (last) red[kHeads * 2 + half * kHeads + h] = l;
+                if (!wg_sync()) break;
+                if (tid == 0 && mbar_wait_fast<true>(&bars->p_empty[buf],
+                                                     ((k / kMsgSlots) & 1) ^ 1, abort_flag,
+                                                     a.status)) {
+                    bulk_s2s(msg_peer + buf * kMsgBytes, smem_u32(mb), kMsgBytes,
+                             pfull_peer + 8 * buf);
+                    bulk_commit();
+                }
                 if (last) {
-                    // ---- segment done: normalised partial and its lse
-                    if (!mbar_wait(&bars->p_empty, k & 1, abort_flag, a.status)) break;
-                    tc_fence_after();
-                    const size_t slot = (size_t)g + b;
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
-                    float* dst = a.o_part + (slot * kHeads + h) * kDL + 256 * rank;
-                    uint32_t r[16];
-                    for (int c = 0; c < 256; c += 16) {
-                        MLA_TMEM_LD_X16(tmem + lane_off + kColO + c, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *(float4*)(dst + c + i) =
-                                make_float4(__uint_as_float(r[i]) * inv,
-                                            __uint_as_float(r[i + 1]) * inv,
-                                            __uint_as_float(r[i + 2]) * inv,
-                                            __uint_as_float(r[i + 3]) * inv);
+                    if (half == 0) {
+                        const float lt = l + red[kHeads * 3 + h];
+                        a.lse_part[((size_t)g + b) * kHeads + h] =
+                            lt > 0.f ? (m + __log2f(lt)) * 0.6931471805599453f : -INFINITY;
                     }
-                    if (rank == 0)
-                        a.lse_part[slot * kHeads + h] =
-                            l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-                    tc_fence_before();
-                    mbar_arrive(&bars->o_free);
                     m = -INFINITY;
                     l = 0.f;
                 }
             }
+            if (tid == 0) bulk_wait_all();
+        } else {
+            // ------------------------------------------ value-CTA warpgroup:
+            // rare O rescales, zeroing of rows past a sequence end, the
+            // normalised partial at the end of a range (thread: head h,
+            // latent columns [256 half, 256 half + 256))
+            const uint32_t pempty_peer = mapa(smem_u32(&bars->p_empty[0]), 0);
+            const uint32_t col0 = kColO + 256 * half;
+            int c = 0;
+            for (int k = 0; k < K; ++k, cur.next()) {
+                const int slot = k % kMsgSlots;
+                const bool first = cur.first(lo), last = cur.last(hi);
+                const int b = cur.b;
+                if (!mbar_wait_fast<true>(&bars->p_full[slot], (k / kMsgSlots) & 1, abort_flag,
+                                          a.status))
+                    break;
+                const float* aux = (const float*)(msg + slot * kMsgBytes + kPBytes);
+                const int* auxi = (const int*)aux;
+                const float alpha = aux[kAuxAlpha + h];
+                const bool need_resc = !first && (auxi[kAuxFlags] | auxi[kAuxFlags + 1] |
+                                                  auxi[kAuxFlags + 2] | auxi[kAuxFlags + 3]) != 0;
+                const int v0 = auxi[kAuxValid], v1 = auxi[kAuxValid + 1];
+                float inv_l = 0.f;
+                if (last) {
+                    const float lt = aux[kAuxSum + h] + aux[kAuxSum + kHeads + h];
+                    inv_l = lt > 0.f ? 1.f / lt : 0.f;
+                }
+                bool ok = true;
+                if (need_resc) {
+                    // O must hold every earlier tile of this range: PV(k-1) done
+                    const int pk_ = k - 1;
+                    ok = mbar_wait_fast(&bars->pv_done[pk_ % kMsgSlots], (pk_ / kMsgSlots) & 1,
+                                        abort_flag, a.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                        uint32_t r[32];
+                        for (int cc = 0; cc < 256; cc += 32) {
+                            MLA_TMEM_LD_X32(tmem + lane_off + col0 + cc, r);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            MLA_TMEM_ST_X32(tmem + lane_off + col0 + cc, r);
+                        }
+                        tmem_st_wait();
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&bars->resc_done);
+                }
+                if (v0 < kHalf || v1 < kHalf) {
+                    // rows past the sequence end (or on an invalid page) hold
+                    // arbitrary bytes: zero them so 0 * garbage cannot reach O
+                    for (int j = 0; j < kVChunks && ok; ++j) {
+                        const int cj = c + j, s = cj % kVSlots, pg = j & 1;
+                        const int valid = pg ? v1 : v0;
+                        if (valid >= kHalf) continue;
+                        ok = mbar_wait_fast(&bars->cfull[s], (cj / kVSlots) & 1, abort_flag,
+                                            a.status);
+                        if (!ok) break;
+                        uint8_t* st = ring + s * kVChunk;
+                        const int rows = kHalf - valid;
+                        for (int e = tid; e < rows * 4 * 8; e += 256) {
+                            const int box = e / (rows * 8), rem = e % (rows * 8);
+                            const int row = valid + rem / 8, ch = rem % 8;
+                            *(uint4*)(st + box * kBox + row * 128 + ch * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    if (!ok) break;
+                    fence_proxy_async();
+                    mbar_arrive(&bars->zeroed);
+                }
+                c += kVChunks;
+                if (!mbar_wait_fast(&bars->pv_done[slot], (k / kMsgSlots) & 1, abort_flag,
+                                    a.status))
+                    break;
+                if (last) {
+                    // ---- the range's normalised partial.  A warp holds a
+                    // 32-head x 32-column block per TMEM load (one row per
+                    // thread); it goes through 4 KB of the consumed message slot
+                    // so that each store instruction writes whole 128-byte rows.
+                    tc_fence_after();
+                    float* xb = (float*)(msg + slot * kMsgBytes) + (warp - 2) * 1024;
+                    float* dst0 = a.o_part + (((size_t)g + b) * kHeads + q4 * 32) * kDL +
+                                  256 * half;
+                    uint32_t r[32];
+                    for (int cc = 0; cc < 256; cc += 32) {
+                        MLA_TMEM_LD_X32(tmem + lane_off + col0 + cc, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            *(float4*)(xb + lane * 32 + 4 * (i ^ (lane & 7))) =
+                                make_float4(__uint_as_float(r[4 * i]) * inv_l,
+                                            __uint_as_float(r[4 * i + 1]) * inv_l,
+                                            __uint_as_float(r[4 * i + 2]) * inv_l,
+                                            __uint_as_float(r[4 * i + 3]) * inv_l);
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int rr = 4 * i + (lane >> 3), ch = lane & 7;
+                            *(float4*)(dst0 + (size_t)rr * kDL + cc + 4 * ch) =
+                                *(const float4*)(xb + rr * 32 + 4 * (ch ^ (rr & 7)));
+                        }
+                        __syncwarp();
+                    }
+                    fence_proxy_async();   // the next bulk copy into this slot comes after
+                    tc_fence_before();
+                    mbar_arrive(&bars->o_free);
+                }
+                // the message slot (P and its factors) may be overwritten now
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(pempty_peer + 8 * slot);
+            }
         }
     }
 
+    pdl_launch_dependents();
     tc_fence_before();
     __syncwarp();
     __syncthreads();
@@ -426,27 +722,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+struct DeviceState {
+    bool init = false;
+    bool attr = false;
+    int major = 0;
+    int workers = 0;
+};
+constexpr int kMaxDev = 64;
+DeviceState g_dev[kMaxDev];
+
+DeviceState* device_state() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+    DeviceState& d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess)
+            return nullptr;
+        d.attr = cudaFuncSetAttribute(decode_tc_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kSmemBytes) == cudaSuccess;
+        cudaGetLastError();
+        d.init = true;
+    }
+    return &d;
+}
+
 }  // namespace
 
 bool decode_tc_supported(int heads, int d_latent, int d_rope, int block_size, int dtype,
                          int batch) {
     if (heads != kHeads || d_latent != kDL || d_rope != kDR || dtype != MLA_DTYPE_BF16)
         return false;
-    if (block_size % kT != 0 || batch > kMaxBatch) return false;
-    int dev = 0, major = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
-        return false;
-    return major >= 10;
+    if (block_size % kHalf != 0 || batch > kMaxBatch) return false;
+    DeviceState* d = device_state();
+    return d && d->major >= 10 && d->attr;
 }
 
+int decode_tc_tile() { return kT; }
+
 // Clusters that can be resident at once (pairs of SMs within one GPC), at most
-// one per SM pair.
+// one per SM pair.  Computed once per device.
 int decode_tc_workers(int num_sms) {
     int w = num_sms / 2 > 0 ? num_sms / 2 : 1;
-    if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-        return w;
+    DeviceState* d = device_state();
+    if (!d || !d->attr) return w;
+    if (d->workers > 0) return d->workers;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * w);
     cfg.blockDim = dim3(kThreads);
@@ -456,33 +777,51 @@ int decode_tc_workers(int num_sms) {
         n < w)
         w = n;
     cudaGetLastError();   // a refused query is not an error of the caller's
+    d->workers = w;
     return w;
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
     if ((uint64_t)a.num_blocks * a.block_size > 0x7fffffffull) return cudaErrorInvalidValue;
-    if (!a.cache || ((uintptr_t)a.q_lat & 15) || ((uintptr_t)a.q_pe & 15))
+    if (!a.cache || ((uintptr_t)a.q_lat & 15) || ((uintptr_t)a.q_pe & 15) || a.tile != kT)
         return cudaErrorInvalidValue;
-    CUtensorMap t_lat, t_rope;
+    DeviceState* d = device_state();
+    if (!d || !d->attr) return cudaErrorNotSupported;
+    CUtensorMap t_cache, t_cache2, t_page, t_qlat, t_qpe;
     const uint64_t rows = (uint64_t)a.num_blocks * a.block_size;
+    // cache rows, 64 x 64 boxes
     const uint64_t dims[2] = {(uint64_t)kD, rows};
     const uint64_t strides[1] = {(uint64_t)kD * 2};
-    const uint32_t box_lat[2] = {64, kT};
-    const uint32_t box_rope[2] = {32, kT};
-    if (!make_tmap_bf16(&t_lat, a.cache, 2, dims, strides, box_lat, 128))
+    const uint32_t box[2] = {64, kHalf};
+    const uint32_t box2[2] = {64, kT};
+    // the same rows seen as [64-column group][row][64 columns]: one box holds
+    // 64 rows of four groups, each group a 128-byte-swizzled 64 x 64 tile
+    const uint64_t dims3[3] = {64, rows, (uint64_t)kD / 64};
+    const uint64_t strides3[2] = {(uint64_t)kD * 2, 128};
+    const uint32_t box3[3] = {64, kHalf, 4};
+    // queries: [batch * heads] rows of 512 latent / 64 rotary values
+    const uint64_t qrows = (uint64_t)a.batch * kHeads;
+    const uint64_t dq[2] = {(uint64_t)kDL, qrows}, sq[1] = {(uint64_t)kDL * 2};
+    const uint64_t dp[2] = {(uint64_t)kDR, qrows}, sp[1] = {(uint64_t)kDR * 2};
+    const uint32_t bq[2] = {64, kHeads};
+    if (!make_tmap_bf16(&t_cache, a.cache, 2, dims, strides, box, 128) ||
+        !make_tmap_bf16(&t_cache2, a.cache, 2, dims, strides, box2, 128) ||
+        !make_tmap_bf16(&t_page, a.cache, 3, dims3, strides3, box3, 128) ||
+        !make_tmap_bf16(&t_qlat, a.q_lat, 2, dq, sq, bq, 128) ||
+        !make_tmap_bf16(&t_qpe, a.q_pe, 2, dp, sp, bq, 128))
         return cudaErrorInvalidValue;
-    if (!make_tmap_bf16(&t_rope, a.cache, 2, dims, strides, box_rope, 64))
-        return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    decode_tc_kernel<<<2 * a.workers, kThreads, kSmemBytes, st>>>(t_lat, t_rope, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * a.workers);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel, t_cache, t_cache2, t_page, t_qlat, t_qpe,
+                              a);
 }
 
 }  // namespace mla

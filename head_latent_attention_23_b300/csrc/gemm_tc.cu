@@ -56,6 +56,9 @@ __global__ void __launch_bounds__(192, 1)
         tmem_alloc(tslot, kBN);
         tmem_relinquish();
     }
+    // set-up above overlaps the previous kernel's tail; operands are read
+    // only once it has finished
+    pdl_wait_primary();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -175,6 +178,7 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
     }
+    pdl_launch_dependents();
     tc_fence_before();
     __syncwarp();
     __syncthreads();
@@ -194,17 +198,28 @@ cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmP
     if (!make_tmap_bf16(&ta, A.ptr, 3, A.dims, A.strides, boxA, 128)) return cudaErrorInvalidValue;
     if (!make_tmap_bf16(&tb, B.ptr, 3, B.dims, B.strides, p.b_mn ? boxBn : boxBk, 128))
         return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
+    // the shared-memory opt-in is a per-device setting
+    static bool attr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr[dev]) {
         cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr[dev] = true;
     }
-    dim3 grid((p.N + kBN - 1) / kBN, (p.M + kBM - 1) / kBM, batch);
-    gemm_tc_kernel<<<grid, 192, kSmemBytes, st>>>(ta, tb, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.N + kBN - 1) / kBN, (p.M + kBM - 1) / kBM, batch);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, ta, tb, p);
 }
 
 }  // namespace mla

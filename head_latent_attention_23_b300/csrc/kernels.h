@@ -12,6 +12,7 @@ namespace mla {
 struct DecodeArgs {
     int heads, d_latent, d_rope, block_size, max_blocks, batch;
     int workers;            // W: tile ranges the context is split into
+    int tile;               // tokens per tile of the split plan
     int64_t num_blocks;
     float scale;
     const void* q_lat;      // [batch][heads][d_latent]
@@ -34,6 +35,7 @@ size_t decode_simt_smem(const DecodeArgs& a);
 // the shapes do not fit it.
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 int decode_tc_workers(int num_sms);
+int decode_tc_tile();   // tokens per tile of the tensor-core kernel's split plan
 bool decode_tc_supported(int heads, int d_latent, int d_rope, int block_size, int dtype,
                          int batch);
 

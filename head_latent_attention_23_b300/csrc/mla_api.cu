@@ -68,8 +68,11 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
 constexpr int kMaxDecodeBatch = 8192;
 
+// The tensor-core kernel takes the maximum of the raw scores, which needs a
+// positive softmax scale; other scales go to the CUDA-core kernel.
 bool use_tc(const mla_config* c, int batch) {
-    return decode_tc_supported(c->heads, c->d_latent, c->d_rope, c->block_size, c->dtype, batch);
+    return c->softmax_scale > 0.f &&
+           decode_tc_supported(c->heads, c->d_latent, c->d_rope, c->block_size, c->dtype, batch);
 }
 
 // Split-KV worker count of the decode kernel that (c, batch) selects.
@@ -251,6 +254,7 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
                           align256(slots * cfg->heads * cfg->d_latent * sizeof(float)));
     cudaStream_t st = (cudaStream_t)stream;
     const bool tc = use_tc(cfg, batch) && al16(q_lat) && al16(q_pe) && al16(cache);
+    a.tile = tc ? decode_tc_tile() : kTile;
     cudaError_t e = tc ? launch_decode_tc(a, st) : launch_decode_simt(a, cfg->dtype, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return cuda_rc(launch_combine_planned(a, cfg->dtype, st));
@@ -450,6 +454,7 @@ extern "C" int mla_decode_noalloc(const mla_config* cfg, const void* q_lat, cons
                           align256(slots * cfg->heads * cfg->d_latent * sizeof(float)));
     cudaStream_t st = (cudaStream_t)stream;
     const bool tc = use_tc(cfg, batch) && al16(q_lat) && al16(q_pe) && al16(cache);
+    a.tile = tc ? decode_tc_tile() : kTile;
     cudaError_t e = tc ? launch_decode_tc(a, st) : launch_decode_simt(a, cfg->dtype, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return cuda_rc(launch_combine_planned(a, cfg->dtype, st));

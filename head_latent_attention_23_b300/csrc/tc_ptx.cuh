@@ -76,6 +76,53 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t addr, uint32_t parity
     return ok != 0;
 }
 
+// Hot-path polls: try_wait without a suspend-time hint (the hardware picks a
+// short, system-dependent limit), so a waiter resumes as soon as the phase
+// completes, whoever completed it.
+__device__ __forceinline__ bool mbar_poll(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_poll_cluster(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait without suspend hints, for the per-tile handshakes of the
+// decode pipeline.  Same give-up rule as mbar_wait.
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, int* status) {
+    const uint32_t a = smem_u32(bar);
+    if (kCluster ? mbar_poll_cluster(a, parity) : mbar_poll(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (kCluster ? mbar_poll_cluster(a, parity) : mbar_poll(a, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                flag(status, MLA_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait for the phase of `bar` with parity `parity` to complete.
 // `abort` is a CTA-shared flag: once any waiter times out, everyone bails.
 template <bool kCluster = false>
@@ -123,6 +170,34 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
                  "f"(c), "f"(d)
                  : "memory");
+}
+// Asynchronous 16-byte store into a peer CTA's shared memory that counts its
+// bytes on the peer's mbarrier (complete_tx); both addresses from mapa.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(addr),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+        : "memory");
+}
+// Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)ptr), "r"(bytes)
+                 : "memory");
+}
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue / wait until the previous kernel's writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
@@ -201,6 +276,15 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// Shared memory -> TMEM copy of a 128-row x 32-byte slice described by a
+// shared-memory matrix descriptor (one k-step of a K-major bf16 operand), to
+// columns [taddr, taddr + 8) of the 128 lanes.  Ordered with this thread's
+// other tcgen05 operations.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator.
 // a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
@@ -237,6 +321,30 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),            \
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                                                 \
         : "r"(taddr))
+
+#define MLA_TMEM_LD_X32(taddr, r)                                                             \
+    asm volatile(                                                                             \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"   \
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),  \
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),          \
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),       \
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),       \
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),       \
+          "=r"(r[31])                                                                         \
+        : "r"(taddr))
+
+#define MLA_TMEM_ST_X32(taddr, r)                                                              \
+    asm volatile(                                                                              \
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"    \
+        ::"r"(taddr),                                                                          \
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), \
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),      \
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),    \
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),    \
+        "r"(r[29]), "r"(r[30]), "r"(r[31])                                                     \
+        : "memory")
 
 #define MLA_TMEM_ST_X16(taddr, r)                                                                \
     asm volatile(                                                                                \
