@@ -129,32 +129,44 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(
     __syncwarp();
 
     T* out = o_lat + ((size_t)b * heads + h) * DL;
-    if ((DL & 3) == 0) {
-        for (int j = lane * 4; j < DL; j += 128) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            int s = 0;
-            for (; s + 1 < ns; s += 2) {
-                const float w0 = wts[warp][s] * inv, w1 = wts[warp][s + 1] * inv;
-                const float4 v0 = *(const float4*)(row_at(s) + j);
-                const float4 v1 = *(const float4*)(row_at(s + 1) + j);
-                if (w0 != 0.f) {
-                    acc.x = fmaf(w0, v0.x, acc.x); acc.y = fmaf(w0, v0.y, acc.y);
-                    acc.z = fmaf(w0, v0.z, acc.z); acc.w = fmaf(w0, v0.w, acc.w);
-                }
-                if (w1 != 0.f) {
-                    acc.x = fmaf(w1, v1.x, acc.x); acc.y = fmaf(w1, v1.y, acc.y);
-                    acc.z = fmaf(w1, v1.z, acc.z); acc.w = fmaf(w1, v1.w, acc.w);
+    if ((DL & 3) == 0 && DL <= 512) {
+        // lane: columns 4 * lane + 128 * q, q < DL / 128 (at most 4 float4).
+        // Eight partials at a time, every load of a batch issued before the
+        // first multiply, so a warp waits for memory once per batch.
+        const int nq = (DL + 127) / 128;
+        float4 acc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < ns; s0 += 8) {
+            float4 v[8][4];
+            float w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int si = s0 + i;
+                w[i] = si < ns ? wts[warp][si] * inv : 0.f;
+                const float* row = si < ns ? row_at(si) : nullptr;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = 4 * lane + 128 * q;
+                    v[i][q] = (row && w[i] != 0.f && q < nq && j < DL)
+                                  ? *(const float4*)(row + j)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
-            if (s < ns) {
-                const float w0 = wts[warp][s] * inv;
-                const float4 v0 = *(const float4*)(row_at(s) + j);
-                if (w0 != 0.f) {
-                    acc.x = fmaf(w0, v0.x, acc.x); acc.y = fmaf(w0, v0.y, acc.y);
-                    acc.z = fmaf(w0, v0.z, acc.z); acc.w = fmaf(w0, v0.w, acc.w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[q].x = fmaf(w[i], v[i][q].x, acc[q].x);
+                    acc[q].y = fmaf(w[i], v[i][q].y, acc[q].y);
+                    acc[q].z = fmaf(w[i], v[i][q].z, acc[q].z);
+                    acc[q].w = fmaf(w[i], v[i][q].w, acc[q].w);
                 }
-            }
-            store4<T>(out + j, acc.x, acc.y, acc.z, acc.w);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = 4 * lane + 128 * q;
+            if (q < nq && j < DL) store4<T>(out + j, acc[q].x, acc[q].y, acc[q].z, acc[q].w);
         }
     } else {
         for (int j = lane; j < DL; j += 32) {

@@ -24,9 +24,11 @@
 //   - the value CTA (rank 1) keeps O in all 512 TMEM columns and computes
 //     O += P C (M=128, N=256, K=128: 16 MMAs) from its own copy of the tile's
 //     latent columns.
-// Each CTA streams what it needs with TMA (128-byte swizzle): the score CTA
-// takes all 576 columns of a tile in nine 64-column chunks of 128 tokens (two
-// 64-row boxes each, since the two pages of a tile need not be adjacent), the
+// Each CTA streams what it needs with TMA (128-byte swizzle), in large boxes
+// because a TMA box costs a roughly fixed time on top of its bytes: the score
+// CTA takes all 576 columns of a tile in three 48 KB chunks of three 64-column
+// groups x 128 tokens (one box of a 3-D [group][row][column] view of the cache
+// when the tile's two pages are adjacent in the pool, else 64-row boxes), the
 // value CTA takes the 512 latent columns in four (column half, page) chunks,
 // each one box of 64 rows x four 64-column groups of a 3-D view of the cache,
 // which hit L2 right after the score CTA brought them in.  Only P crosses the
@@ -58,23 +60,27 @@ constexpr int kHeads = 128, kDL = 512, kDR = 64, kD = kDL + kDR;
 constexpr int kT = 128;                  // tokens per tile
 constexpr int kHalf = 64;                // rows per TMA box (a tile = two boxes)
 constexpr int kBox = kHalf * 64 * 2;     // 8 KB: 64 rows x 64 columns
-// score CTA ring: 64 columns x 128 tokens per chunk, nine chunks per tile
-constexpr int kSChunk = 2 * kBox;
-constexpr int kSChunks = 9;
-constexpr int kSSlots = 8;
+// score CTA ring: chunks of three 64-column groups x 128 tokens (48 KB), three
+// chunks per tile (576 columns = 9 groups); a group's tile is 128 rows x 128 B
+constexpr int kGroup = 2 * kBox;             // 16 KB: one 64-column group, 128 rows
+constexpr int kSGroups = 3;                  // groups per chunk
+constexpr int kSChunk = kSGroups * kGroup;   // 48 KB
+constexpr int kSChunks = 3;                  // chunks per tile
+constexpr int kSSlots = 3;
 // value CTA ring: 256 columns x 64 tokens per chunk, four chunks per tile
 constexpr int kVChunk = 4 * kBox;
 constexpr int kVChunks = 4;
 constexpr int kVSlots = 4;
 constexpr int kRingBytes = kSSlots * kSChunk;
-static_assert(kRingBytes == kVSlots * kVChunk, "one ring region for both roles");
+static_assert(kRingBytes >= kVSlots * kVChunk, "one ring region for both roles");
 // message: P [128 heads x 128 tokens] bf16 as two K-major 128-byte-swizzled
 // blocks of 64 tokens, then the per-head factors
 constexpr int kPBytes = kHeads * kT * 2;   // 32 KB
 constexpr int kAuxBytes = 2048;    // factors, row sums, flags, valid rows
 constexpr int kMsgBytes = kPBytes + kAuxBytes;
 constexpr int kMsgSlots = 2;             // value CTA: two receive slots
-constexpr int kQChunks = 8;              // latent query: eight 128-head x 64-column chunks
+constexpr int kQGroups = 8;              // latent query: eight 64-column groups of 128 heads
+constexpr int kQChunks = 3;              // ... in chunks of three groups (the last has two)
 constexpr int kQpeBytes = kHeads * kDR * 2;   // 16 KB
 constexpr int kMaxBatch = 1024;
 // The score CTA stages one outgoing message at kMsgOff and keeps the rotary
@@ -107,7 +113,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 struct Bars {
-    uint64_t cfull[8], cempty[8];           // chunk ring
+    uint64_t cfull[4], cempty[4];           // chunk ring
     uint64_t s_full[2], s_empty[2];         // score CTA: S double buffer
     uint64_t qpe_full[2], qpe_free[2];      // score CTA: rotary query of a range
     uint64_t p_empty[kMsgSlots];            // score CTA: value CTA freed a message slot
@@ -193,7 +199,7 @@ __device__ __forceinline__ void bulk_wait_all() {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap t_cache,
-                     const __grid_constant__ CUtensorMap t_cache2,
+                     const __grid_constant__ CUtensorMap t_chunk,
                      const __grid_constant__ CUtensorMap t_page,
                      const __grid_constant__ CUtensorMap t_qlat,
                      const __grid_constant__ CUtensorMap t_qpe,
@@ -214,7 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int cap = a.max_blocks * a.block_size;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 8; ++s) {
+        for (int s = 0; s < 4; ++s) {
             mbar_init(&bars->cfull[s], 1);
             mbar_init(&bars->cempty[s], 1);
         }
@@ -237,7 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bars->abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&t_cache);
-        prefetch_tmap(&t_cache2);
+        prefetch_tmap(&t_chunk);
         prefetch_tmap(&t_page);
         prefetch_tmap(&t_qlat);
         prefetch_tmap(&t_qpe);
@@ -293,10 +299,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     &bars->qpe_full[qb]);
                         ++seg;
                         for (int j = 0; j < kQChunks && ok; ++j, ++c) {
+                            // three groups per box; the last box's third group
+                            // lies past the query row and is zero-filled
                             const int s = ring_slot(kSSlots, kSChunk);
                             if (s < 0) break;
-                            tma_load_2d(ring + s * kSChunk, &t_qlat, 64 * j, cur.b * kHeads,
-                                        &bars->cfull[s]);
+                            tma_load_3d(ring + s * kSChunk, &t_qlat, 0, cur.b * kHeads,
+                                        kSGroups * j, &bars->cfull[s]);
                         }
                         if (!ok) break;
                     }
@@ -309,10 +317,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (s < 0) break;
                         uint8_t* dst = ring + s * kSChunk;
                         if (adjacent) {
-                            tma_load_2d(dst, &t_cache2, 64 * j, tr.row[0], &bars->cfull[s]);
+                            tma_load_3d(dst, &t_chunk, 0, tr.row[0], kSGroups * j, &bars->cfull[s]);
                         } else {
-                            tma_load_2d(dst, &t_cache, 64 * j, tr.row[0], &bars->cfull[s]);
-                            tma_load_2d(dst + kBox, &t_cache, 64 * j, tr.row[1], &bars->cfull[s]);
+                            for (int gg = 0; gg < kSGroups; ++gg) {
+                                const int x = 64 * (kSGroups * j + gg);
+                                tma_load_2d(dst + gg * kGroup, &t_cache, x, tr.row[0],
+                                            &bars->cfull[s]);
+                                tma_load_2d(dst + gg * kGroup + kBox, &t_cache, x, tr.row[1],
+                                            &bars->cfull[s]);
+                            }
                         }
                     }
                 } else {
@@ -356,10 +369,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             }
                             tc_fence_after();
                             const uint32_t st = smem_u32(ring + s * kSChunk);
+                            for (int gg = 0; gg < kSGroups; ++gg) {
+                                const int qg = kSGroups * j + gg;
+                                if (qg >= kQGroups) break;
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                tmem_cp_128x256b(tmem + kColQ + 32 * j + 8 * kk,
-                                                 sdesc(st + 32 * kk, 16, 1024, 2));
+                                for (int kk = 0; kk < 4; ++kk)
+                                    tmem_cp_128x256b(tmem + kColQ + 32 * qg + 8 * kk,
+                                                     sdesc(st + gg * kGroup + 32 * kk, 16, 1024, 2));
+                            }
                             tc_commit(&bars->cempty[s]);
                         }
                         if (!ok) break;
@@ -385,17 +402,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t st = smem_u32(ring + s * kSChunk);
-                        if (j < kSChunks - 1) {
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ts(d_s, tmem + kColQ + 32 * j + 8 * kk,
-                                       sdesc(st + 32 * kk, 16, 1024, 2), id_s, (j | kk) != 0);
-                        } else {
-                            // rotary part: Q_pe from shared memory
+                        for (int gg = 0; gg < kSGroups; ++gg) {
+                            const int cg = kSGroups * j + gg;     // 64-column group 0..8
+                            const uint32_t gt = st + gg * kGroup;
+                            if (cg < kQGroups) {
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(d_s, sdesc(qa + 32 * kk, 16, 1024, 2),
-                                       sdesc(st + 32 * kk, 16, 1024, 2), id_s, 1);
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_ts(d_s, tmem + kColQ + 32 * cg + 8 * kk,
+                                           sdesc(gt + 32 * kk, 16, 1024, 2), id_s, (cg | kk) != 0);
+                            } else {
+                                // rotary part: Q_pe from shared memory
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_ss(d_s, sdesc(qa + 32 * kk, 16, 1024, 2),
+                                           sdesc(gt + 32 * kk, 16, 1024, 2), id_s, 1);
+                            }
                         }
                         tc_commit(&bars->cempty[s]);
                     }
@@ -787,27 +809,30 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
         return cudaErrorInvalidValue;
     DeviceState* d = device_state();
     if (!d || !d->attr) return cudaErrorNotSupported;
-    CUtensorMap t_cache, t_cache2, t_page, t_qlat, t_qpe;
+    CUtensorMap t_cache, t_chunk, t_page, t_qlat, t_qpe;
     const uint64_t rows = (uint64_t)a.num_blocks * a.block_size;
     // cache rows, 64 x 64 boxes
     const uint64_t dims[2] = {(uint64_t)kD, rows};
     const uint64_t strides[1] = {(uint64_t)kD * 2};
     const uint32_t box[2] = {64, kHalf};
-    const uint32_t box2[2] = {64, kT};
     // the same rows seen as [64-column group][row][64 columns]: one box holds
     // 64 rows of four groups, each group a 128-byte-swizzled 64 x 64 tile
     const uint64_t dims3[3] = {64, rows, (uint64_t)kD / 64};
     const uint64_t strides3[2] = {(uint64_t)kD * 2, 128};
     const uint32_t box3[3] = {64, kHalf, 4};
-    // queries: [batch * heads] rows of 512 latent / 64 rotary values
+    const uint32_t boxc[3] = {64, kT, kSGroups};     // score chunk: 128 rows x 3 groups
+    // queries: [batch * heads] rows of 512 latent / 64 rotary values; the
+    // latent part seen as [group][row][64 columns] like the cache
     const uint64_t qrows = (uint64_t)a.batch * kHeads;
-    const uint64_t dq[2] = {(uint64_t)kDL, qrows}, sq[1] = {(uint64_t)kDL * 2};
+    const uint64_t dq[3] = {64, qrows, (uint64_t)kQGroups};
+    const uint64_t sq[2] = {(uint64_t)kDL * 2, 128};
+    const uint32_t bq3[3] = {64, kHeads, kSGroups};
     const uint64_t dp[2] = {(uint64_t)kDR, qrows}, sp[1] = {(uint64_t)kDR * 2};
     const uint32_t bq[2] = {64, kHeads};
     if (!make_tmap_bf16(&t_cache, a.cache, 2, dims, strides, box, 128) ||
-        !make_tmap_bf16(&t_cache2, a.cache, 2, dims, strides, box2, 128) ||
+        !make_tmap_bf16(&t_chunk, a.cache, 3, dims3, strides3, boxc, 128) ||
         !make_tmap_bf16(&t_page, a.cache, 3, dims3, strides3, box3, 128) ||
-        !make_tmap_bf16(&t_qlat, a.q_lat, 2, dq, sq, bq, 128) ||
+        !make_tmap_bf16(&t_qlat, a.q_lat, 3, dq, sq, bq3, 128) ||
         !make_tmap_bf16(&t_qpe, a.q_pe, 2, dp, sp, bq, 128))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -820,7 +845,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel, t_cache, t_cache2, t_page, t_qlat, t_qpe,
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel, t_cache, t_chunk, t_page, t_qlat, t_qpe,
                               a);
 }
 

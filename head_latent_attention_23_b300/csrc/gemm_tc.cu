@@ -6,10 +6,12 @@
 //
 //   C[z][m][n] = sum_k A[z][m][k] * B[z][k][n]
 //
-// One CTA computes a 128 x 128 tile of C.  Warp 0 streams 64-deep k slices
-// of A (K-major) and B (K-major or N-major) into a 4-stage ring with TMA
-// (128-byte swizzle); one thread of warp 1 issues tcgen05.mma (M=128, N=128,
-// K=16) into a TMEM accumulator; warps 2-5 drain TMEM through registers.
+// 128 x 128 tiles of C, K in 64-deep slices of A (K-major) and B (K-major or
+// N-major) streamed into a 4-stage ring with TMA (128-byte swizzle);
+// tcgen05.mma (M=128, N=128, K=16) accumulates in TMEM.  The kernel is
+// persistent (at most one CTA per SM, looping over tiles) so that, at decode
+// batch sizes where a tile is a few k slices, the weight stream never stops
+// for a CTA's set-up or epilogue.
 #include "kernels.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -21,30 +23,53 @@ namespace {
 constexpr int kBM = 128, kBN = 128, kBK = 64, kStages = 4;
 constexpr int kTileBytes = 16384;   // one 128 x 64 bf16 slice of A or of B
 constexpr int kSmemBytes = 1024 + kStages * 2 * kTileBytes + 256;
+constexpr int kAcc = 2;             // TMEM accumulators: the epilogue drains one tile
+                                    // while the MMAs fill the other
 
 using namespace tc;
 
+// Output tile `t` of the (n, m, z) grid of 128 x 128 tiles.
+struct TileId {
+    int n0, m0, z;
+};
+__device__ __forceinline__ TileId tile_of(int t, int tiles_n, int tiles_m) {
+    TileId r;
+    r.n0 = (t % tiles_n) * kBN;
+    r.m0 = ((t / tiles_n) % tiles_m) * kBM;
+    r.z = t / (tiles_n * tiles_m);
+    return r;
+}
+
+// Persistent: CTA c takes tiles c, c + gridDim.x, ...  Warp 0 streams the k
+// slices of all its tiles through one ring; one thread of warp 1 accumulates
+// each tile into one of two TMEM buffers; warps 2-5 drain a finished buffer
+// (128 rows = TMEM lanes) while the next tile is being computed.
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
-                   const TcGemmParams p) {
+                   const TcGemmParams p, int tiles_n, int tiles_m, int num_tiles) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + kStages * kTileBytes;
     uint64_t* full = (uint64_t*)(sB + kStages * kTileBytes);
     uint64_t* empty = full + kStages;
-    uint64_t* done = empty + kStages;
+    uint64_t* acc_full = empty + kStages;
+    uint64_t* acc_empty = acc_full + kAcc;
+    uint64_t* done = acc_empty + kAcc;
     uint32_t* tslot = (uint32_t*)(done + 1);
     volatile int* abort_flag = (volatile int*)(tslot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM, z = blockIdx.z;
     const int nk = (p.K + kBK - 1) / kBK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < kAcc; ++s) {
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], 128);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
@@ -53,7 +78,7 @@ __global__ void __launch_bounds__(192, 1)
         prefetch_tmap(&tB);
     }
     if (warp == 1) {
-        tmem_alloc(tslot, kBN);
+        tmem_alloc(tslot, kAcc * kBN);
         tmem_relinquish();
     }
     // set-up above overlaps the previous kernel's tail; operands are read
@@ -66,43 +91,65 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            int issued = 0;
-            for (int kt = 0; kt < nk; ++kt) {
-                const int s = kt % kStages;
-                if (!mbar_wait(&empty[s], ((kt / kStages) & 1) ^ 1, abort_flag, p.status)) break;
-                mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
-                tma_load_3d(sA + s * kTileBytes, &tA, kt * kBK, m0, z, &full[s]);
-                if (p.b_mn) {
-                    tma_load_3d(sB + s * kTileBytes, &tB, n0, kt * kBK, z, &full[s]);
-                    tma_load_3d(sB + s * kTileBytes + kTileBytes / 2, &tB, n0 + 64, kt * kBK, z,
-                                &full[s]);
-                } else {
-                    tma_load_3d(sB + s * kTileBytes, &tB, kt * kBK, n0, z, &full[s]);
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileId ti = tile_of(t, tiles_n, tiles_m);
+                for (int kt = 0; kt < nk; ++kt, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait_fast(&empty[s], ((it / kStages) & 1) ^ 1, abort_flag,
+                                        p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
+                    tma_load_3d(sA + s * kTileBytes, &tA, kt * kBK, ti.m0, ti.z, &full[s]);
+                    if (p.b_mn) {
+                        tma_load_3d(sB + s * kTileBytes, &tB, ti.n0, kt * kBK, ti.z, &full[s]);
+                        tma_load_3d(sB + s * kTileBytes + kTileBytes / 2, &tB, ti.n0 + 64,
+                                    kt * kBK, ti.z, &full[s]);
+                    } else {
+                        tma_load_3d(sB + s * kTileBytes, &tB, kt * kBK, ti.n0, ti.z, &full[s]);
+                    }
                 }
-                issued = kt + 1;
             }
             // every copy this thread started has landed before the CTA exits
-            for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt)
-                drain_wait(&full[kt % kStages], (kt / kStages) & 1);
+            for (int i = it > kStages ? it - kStages : 0; i < it; ++i)
+                drain_wait(&full[i % kStages], (i / kStages) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(kBM, kBN, false, p.b_mn != 0);
-            for (int kt = 0; kt < nk; ++kt) {
-                const int s = kt % kStages;
-                if (!mbar_wait(&full[s], (kt / kStages) & 1, abort_flag, p.status)) break;
+            int it = 0, lt = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++lt) {
+                const int ab = lt % kAcc;
+                if (!mbar_wait_fast(&acc_empty[ab], ((lt / kAcc) & 1) ^ 1, abort_flag, p.status))
+                    break;
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(sA + s * kTileBytes);
-                const uint32_t b0 = smem_u32(sB + s * kTileBytes);
+                const uint32_t d = tmem + (uint32_t)(ab * kBN);
+                for (int kt = 0; kt < nk; ++kt, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait_fast(&full[s], (it / kStages) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + s * kTileBytes);
+                    const uint32_t b0 = smem_u32(sB + s * kTileBytes);
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k) {
-                    const uint64_t ad = sdesc(a0 + 32 * k, 16, 1024, 2);
-                    const uint64_t bd = p.b_mn ? sdesc(b0 + 2048 * k, kTileBytes / 2, 1024, 2)
-                                               : sdesc(b0 + 32 * k, 16, 1024, 2);
-                    mma_ss(tmem, ad, bd, idesc, (kt | k) != 0);
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        const uint64_t ad = sdesc(a0 + 32 * k, 16, 1024, 2);
+                        const uint64_t bd = p.b_mn ? sdesc(b0 + 2048 * k, kTileBytes / 2, 1024, 2)
+                                                   : sdesc(b0 + 32 * k, 16, 1024, 2);
+                        mma_ss(d, ad, bd, idesc, (kt | k) != 0);
+                    }
+                    tc_commit(&empty[s]);
                 }
-                tc_commit(&empty[s]);
+                if (!ok) break;
+                tc_commit(&acc_full[ab]);
             }
+            // every MMA this thread issued has finished before the CTA exits
             tc_commit(done);
             drain_wait(done, 0);
         }
@@ -110,11 +157,16 @@ __global__ void __launch_bounds__(192, 1)
         // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = tile rows
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        const int m = m0 + row;
-        bool ok = mbar_wait(done, 0, abort_flag, p.status);
-        ok = __all_sync(0xffffffffu, ok);
-        tc_fence_after();
-        if (ok) {
+        int lt = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
+            const int ab = lt % kAcc;
+            const TileId ti = tile_of(t, tiles_n, tiles_m);
+            const int n0 = ti.n0, z = ti.z;
+            const int m = ti.m0 + row;
+            bool ok = mbar_wait_fast(&acc_full[ab], (lt / kAcc) & 1, abort_flag, p.status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
             int64_t slot = -1;
             if (p.epi == 1 && m < p.M) {
                 const int b = p.seq_idx[m], ps = p.pos[m];
@@ -125,10 +177,11 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 if (slot < 0 && n0 == 0) flag(p.status, MLA_ERR_INDEX);
             }
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kBN);
             for (int c = 0; c < kBN; c += 16) {
                 uint32_t r[16];
                 __syncwarp();
-                MLA_TMEM_LD_X16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, r);
+                MLA_TMEM_LD_X16(taddr + (uint32_t)c, r);
                 tmem_ld_wait();
                 if (m >= p.M) continue;
                 float v[16];
@@ -165,9 +218,17 @@ __global__ void __launch_bounds__(192, 1)
                     const int64_t base = (int64_t)z * p.sCz + (int64_t)m * p.sCm + nb;
                     if (p.c_dtype == MLA_DTYPE_BF16) {
                         __nv_bfloat16* C = (__nv_bfloat16*)p.C + base;
+                        if (nb + 16 <= p.N && ((uintptr_t)C & 15) == 0) {
+                            uint32_t w[8];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (nb + i < p.N) C[i] = __float2bfloat16_rn(v[i]);
+                            for (int i = 0; i < 8; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+                            *(uint4*)C = make_uint4(w[0], w[1], w[2], w[3]);
+                            *(uint4*)(C + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (nb + i < p.N) C[i] = __float2bfloat16_rn(v[i]);
+                        }
                     } else {
                         float* C = (float*)p.C + base;
 #pragma unroll
@@ -176,6 +237,8 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[ab]);
         }
     }
     pdl_launch_dependents();
@@ -183,7 +246,7 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kBN);
+    if (warp == 1) tmem_dealloc(tmem, kAcc * kBN);
 }
 
 }  // namespace
@@ -209,8 +272,16 @@ cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmP
         if (e != cudaSuccess) return e;
         attr[dev] = true;
     }
+    static int sms[64] = {};
+    if (!sms[dev] &&
+        cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const int tiles_n = (p.N + kBN - 1) / kBN, tiles_m = (p.M + kBM - 1) / kBM;
+    const int64_t tiles = (int64_t)tiles_n * tiles_m * batch;
+    if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+    const int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((p.N + kBN - 1) / kBN, (p.M + kBM - 1) / kBM, batch);
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(192);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = st;
@@ -219,7 +290,7 @@ cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmP
     la[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = la;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, ta, tb, p);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, ta, tb, p, tiles_n, tiles_m, (int)tiles);
 }
 
 }  // namespace mla

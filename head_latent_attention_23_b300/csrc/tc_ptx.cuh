@@ -181,6 +181,20 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
         "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
         : "memory");
 }
+__device__ __forceinline__ void st_async_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(addr),
+        "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+        : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+        "r"(v), "r"(remote_bar)
+        : "memory");
+}
 // Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)ptr), "r"(bytes)
