@@ -6,7 +6,7 @@
 // which is exact because exp(lse_s) is the softmax denominator of range s.
 // Empty ranges carry lse = -inf and weigh nothing.
 //
-// One warp per (sequence, head), four heads per CTA: the lanes compute the
+// One warp per (sequence, head), eight heads per CTA: the lanes compute the
 // weights of up to 32 partials at a time with shuffles, then stream the
 // partial rows with 16-byte loads (HBM/L2-bound, no tensor-core work).  The
 // planned variant is launched as a programmatic dependent of the decode
@@ -19,8 +19,8 @@ namespace mla {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kMaxSlots = 1024;
+constexpr int kWarps = 8;        // one head per warp
+constexpr int kMaxSlots = 512;
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -44,59 +44,26 @@ template <typename T, bool kPlanned>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(
     const float* __restrict__ o_part, const float* __restrict__ lse_part, int n_splits,
     int batch, int heads, int DL, T* __restrict__ o_lat, float* __restrict__ lse,
-    const int32_t* __restrict__ seq_lens, int cap, int W, int tile) {
+    const int4* __restrict__ seq_slots, int W) {
     __shared__ int slots[kMaxSlots];
     __shared__ float wts[kWarps][kMaxSlots];
-    __shared__ int red[2][kWarps];
     __shared__ int n_sl;
     const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y * kWarps + warp;
 
     if (kPlanned) {
         pdl_wait();
-        // tiles of the sequences before b, and in all sequences
-        int before = 0, all = 0, mine = 0;
-        for (int j = tid; j < batch; j += blockDim.x) {
-            int n = seq_lens[j];
-            n = (n < 1) ? 0 : (n > cap ? cap : n);
-            const int t = (n + tile - 1) / tile;
-            all += t;
-            if (j < b) before += t;
-            if (j == b) mine = t;
+        // the decode kernel published this sequence's workers [g0, g1]; a worker
+        // with an empty range (only when there are fewer tiles than workers)
+        // wrote no partial and is skipped
+        const int4 info = seq_slots[b];
+        const int g0 = info.x, cnt = info.y - info.x + 1;
+        const int64_t total = (int64_t)(uint32_t)info.z | ((int64_t)info.w << 32);
+        for (int s = tid; s < cnt && s < kMaxSlots; s += blockDim.x) {
+            const int g = g0 + s;
+            slots[s] = plan_lo(g, total, W) < plan_lo(g + 1, total, W) ? g + b : -1;
         }
-        before = __reduce_add_sync(0xffffffffu, before);
-        all = __reduce_add_sync(0xffffffffu, all);
-        mine = __reduce_add_sync(0xffffffffu, mine);
-        if (lane == 0) {
-            red[0][warp] = before;
-            red[1][warp] = all;
-        }
-        __shared__ int sh_mine[kWarps];
-        if (lane == 0) sh_mine[warp] = mine;
-        __syncthreads();
-        if (tid == 0) {
-            int64_t p0 = 0, total = 0;
-            int t_b = 0;
-            for (int w = 0; w < kWarps; ++w) {
-                p0 += red[0][w];
-                total += red[1][w];
-                t_b += sh_mine[w];
-            }
-            const int64_t p1 = p0 + t_b;
-            int cnt = 0;
-            if (p1 > p0) {
-                // workers whose tile range [plan_lo(g), plan_lo(g+1)) meets [p0, p1)
-                int g = (int)(p0 * W / total);
-                while (g > 0 && plan_lo(g, total, W) > p0) --g;
-                while (g + 1 < W && plan_lo(g + 1, total, W) <= p0) ++g;
-                for (; g < W && plan_lo(g, total, W) < p1; ++g) {
-                    const int64_t glo = plan_lo(g, total, W), ghi = plan_lo(g + 1, total, W);
-                    if (ghi <= p0 || glo >= ghi) continue;
-                    if (cnt < kMaxSlots) slots[cnt++] = g + b;
-                }
-            }
-            n_sl = cnt;
-        }
+        if (tid == 0) n_sl = cnt < 0 ? 0 : (cnt < kMaxSlots ? cnt : kMaxSlots);
     } else {
         for (int s = tid; s < n_splits && s < kMaxSlots; s += blockDim.x) slots[s] = s;
         if (tid == 0) n_sl = n_splits < kMaxSlots ? n_splits : kMaxSlots;
@@ -104,11 +71,14 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(
     __syncthreads();
     if (h >= heads) return;
     const int ns = n_sl;
+    // slot -1: a worker without tokens (weight 0, never read)
     auto lse_at = [&](int s) -> float {
+        if (slots[s] < 0) return -INFINITY;
         return kPlanned ? lse_part[(size_t)slots[s] * heads + h]
                         : lse_part[((size_t)slots[s] * batch + b) * heads + h];
     };
     auto row_at = [&](int s) -> const float* {
+        if (slots[s] < 0) return nullptr;
         return kPlanned ? o_part + ((size_t)slots[s] * heads + h) * DL
                         : o_part + (((size_t)slots[s] * batch + b) * heads + h) * DL;
     };
@@ -131,17 +101,17 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(
     T* out = o_lat + ((size_t)b * heads + h) * DL;
     if ((DL & 3) == 0 && DL <= 512) {
         // lane: columns 4 * lane + 128 * q, q < DL / 128 (at most 4 float4).
-        // Eight partials at a time, every load of a batch issued before the
+        // Four partials at a time, every load of a batch issued before the
         // first multiply, so a warp waits for memory once per batch.
         const int nq = (DL + 127) / 128;
         float4 acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < ns; s0 += 8) {
-            float4 v[8][4];
-            float w[8];
+        for (int s0 = 0; s0 < ns; s0 += 4) {
+            float4 v[4][4];
+            float w[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4; ++i) {
                 const int si = s0 + i;
                 w[i] = si < ns ? wts[warp][si] * inv : 0.f;
                 const float* row = si < ns ? row_at(si) : nullptr;
@@ -154,7 +124,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     acc[q].x = fmaf(w[i], v[i][q].x, acc[q].x);
@@ -173,7 +143,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(
             float acc = 0.f;
             for (int s = 0; s < ns; ++s) {
                 const float w = wts[warp][s] * inv;
-                if (w != 0.f) acc = fmaf(w, row_at(s)[j], acc);
+                if (w != 0.f) acc = fmaf(w, row_at(s)[j], acc);   // w == 0 for slot -1
             }
             out[j] = from_f<T>(acc);
         }
@@ -183,8 +153,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(
 
 template <typename T, bool kPlanned>
 cudaError_t launch(const float* o_part, const float* lse_part, int n_splits, int batch,
-                   int heads, int DL, void* o_lat, float* lse, const int32_t* seq_lens, int cap,
-                   int W, int tile, bool pdl, cudaStream_t st) {
+                   int heads, int DL, void* o_lat, float* lse, const int4* seq_slots, int W,
+                   bool pdl, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(batch, (heads + kWarps - 1) / kWarps);
     cfg.blockDim = dim3(kWarps * 32);
@@ -195,19 +165,18 @@ cudaError_t launch(const float* o_part, const float* lse_part, int n_splits, int
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, combine_kernel<T, kPlanned>, o_part, lse_part, n_splits,
-                              batch, heads, DL, (T*)o_lat, lse, seq_lens, cap, W, tile);
+                              batch, heads, DL, (T*)o_lat, lse, seq_slots, W);
 }
 
 }  // namespace
 
 cudaError_t launch_combine_planned(const DecodeArgs& a, int dtype, cudaStream_t st) {
-    const int cap = a.max_blocks * a.block_size;
     if (dtype == MLA_DTYPE_BF16)
         return launch<__nv_bfloat16, true>(a.o_part, a.lse_part, 0, a.batch, a.heads,
-                                           a.d_latent, a.o_lat, a.lse, a.seq_lens, cap,
-                                           a.workers, a.tile, true, st);
+                                           a.d_latent, a.o_lat, a.lse, a.seq_slots, a.workers,
+                                           true, st);
     return launch<float, true>(a.o_part, a.lse_part, 0, a.batch, a.heads, a.d_latent, a.o_lat,
-                               a.lse, a.seq_lens, cap, a.workers, a.tile, true, st);
+                               a.lse, a.seq_slots, a.workers, true, st);
 }
 
 cudaError_t launch_combine_dense(const float* o_part, const float* lse_part, int n_splits,
@@ -216,9 +185,9 @@ cudaError_t launch_combine_dense(const float* o_part, const float* lse_part, int
     if (n_splits > kMaxSlots) return cudaErrorInvalidValue;
     if (dtype == MLA_DTYPE_BF16)
         return launch<__nv_bfloat16, false>(o_part, lse_part, n_splits, batch, heads, d_latent,
-                                            o_lat, lse, nullptr, 0, 1, 1, false, st);
+                                            o_lat, lse, nullptr, 1, false, st);
     return launch<float, false>(o_part, lse_part, n_splits, batch, heads, d_latent, o_lat, lse,
-                                nullptr, 0, 1, 1, false, st);
+                                nullptr, 1, false, st);
 }
 
 }  // namespace mla

@@ -106,6 +106,28 @@ __device__ __forceinline__ void tile_prefix(const int32_t* seq_lens, int batch, 
     __syncthreads();
 }
 
+// Worker whose range [plan_lo(g), plan_lo(g+1)) holds tile t (0 <= t < total):
+// the largest g with floor(g * total / W) <= t.
+__host__ __device__ __forceinline__ int worker_of_tile(int64_t t, int64_t total, int W) {
+    return (int)(((t + 1) * W - 1) / total);
+}
+
+// Publishes, for each sequence, the first and last worker whose range meets it
+// and the total tile count: the merge kernel reads its partial slots from this
+// instead of recomputing the tile prefix.  One CTA of the decode grid calls
+// it (all its threads), after the prefix is in shared memory.
+__device__ __forceinline__ void publish_seq_slots(const int* pre, int batch, int W, int4* out) {
+    const int64_t total = pre[batch];
+    for (int b = threadIdx.x; b < batch; b += blockDim.x) {
+        int4 v = make_int4(0, -1, (int)(total & 0xffffffff), (int)(total >> 32));
+        if (pre[b + 1] > pre[b]) {
+            v.x = worker_of_tile(pre[b], total, W);
+            v.y = worker_of_tile(pre[b + 1] - 1, total, W);
+        }
+        out[b] = v;
+    }
+}
+
 // Index of the sequence holding global tile t: largest b with pre[b] <= t.
 __device__ __forceinline__ int seq_of_tile(const int* pre, int batch, int64_t t) {
     int lo = 0, hi = batch - 1;

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(DecodeArgs a) {
     const int lane = tid & 31, warp = tid >> 5;
     const int cap = a.max_blocks * a.block_size;
     tile_prefix(a.seq_lens, a.batch, cap, pre, a.status);
+    if (blockIdx.x == 0 && blockIdx.y == 0) publish_seq_slots(pre, a.batch, a.workers, a.seq_slots);
     const int64_t total = pre[a.batch];
     const int64_t lo = plan_lo(g, total, a.workers), hi = plan_lo(g + 1, total, a.workers);
     if (lo >= hi) return;

@@ -256,6 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // only once it has finished
     pdl_wait_primary();
     tile_prefix(a.seq_lens, a.batch, cap, pre, scorer ? a.status : nullptr, lens, kT);
+    if (blockIdx.x == 0) publish_seq_slots(pre, a.batch, a.workers, a.seq_slots);
     tc_fence_before();
     cluster_sync();        // both CTAs' barriers exist before any remote access
     tc_fence_after();
@@ -329,6 +330,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
+                    // the first tile's P arrives a full S and softmax after the
+                    // start: holding these loads back until then leaves the
+                    // score CTAs' first (cold) loads a less crowded memory system
+                    if (k == 0 && !mbar_wait_fast<true>(&bars->p_full[0], 0, abort_flag, a.status))
+                        break;
                     // one box per chunk: 64 rows of a page x four 64-column groups
                     for (int j = 0; j < kVChunks && ok; ++j, ++c) {
                         const int s = ring_slot(kVSlots, kVChunk);

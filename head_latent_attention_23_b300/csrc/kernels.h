@@ -22,6 +22,8 @@ struct DecodeArgs {
     const int32_t* seq_lens;
     float* o_part;          // [W + batch][heads][d_latent]
     float* lse_part;        // [W + batch][heads]
+    int4* seq_slots;        // [batch]: first and last worker of each sequence and the
+                            // total tile count, written by the decode kernel for the merge
     void* o_lat;            // [batch][heads][d_latent]
     float* lse;             // [batch][heads] or null
     int* status;

@@ -105,10 +105,24 @@ TcGemmParams gemm_params(int M, int N, int K, bool b_mn, void* C, int64_t sCz, i
     return g;
 }
 
+// Workspace of a decode call: split-KV partials (W + batch slots of
+// heads x d_latent fp32), their log-sum-exps, and per sequence the range of
+// workers that produced its partials (int4).
 size_t decode_ws_bytes(const mla_config* c, int W, int batch) {
     size_t slots = (size_t)W + (size_t)batch;
     return align256(slots * c->heads * c->d_latent * sizeof(float)) +
-           align256(slots * c->heads * sizeof(float));
+           align256(slots * c->heads * sizeof(float)) + align256((size_t)batch * 16);
+}
+
+// Points the partial, lse and slot-range arrays of `a` into `ws`.
+void carve_decode_ws(DecodeArgs& a, const mla_config* c, void* ws, int W, int batch) {
+    const size_t slots = (size_t)W + batch;
+    char* p = (char*)ws;
+    a.o_part = (float*)p;
+    p += align256(slots * c->heads * c->d_latent * sizeof(float));
+    a.lse_part = (float*)p;
+    p += align256(slots * c->heads * sizeof(float));
+    a.seq_slots = (int4*)p;
 }
 
 }  // namespace
@@ -242,16 +256,13 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
     if (!workspace || ws_bytes < need || ((uintptr_t)workspace & 255)) return MLA_ERR_WORKSPACE;
     int* status;
     if (int rc = status_ptr(&status)) return rc;
-    const size_t slots = (size_t)W + batch;
     DecodeArgs a{};
     a.heads = cfg->heads; a.d_latent = cfg->d_latent; a.d_rope = cfg->d_rope;
     a.block_size = cfg->block_size; a.max_blocks = max_blocks; a.batch = batch;
     a.workers = W; a.num_blocks = num_blocks; a.scale = cfg->softmax_scale;
     a.q_lat = q_lat; a.q_pe = q_pe; a.cache = cache; a.block_table = block_table;
     a.seq_lens = seq_lens; a.o_lat = o_lat; a.lse = lse; a.status = status;
-    a.o_part = (float*)workspace;
-    a.lse_part = (float*)((char*)workspace +
-                          align256(slots * cfg->heads * cfg->d_latent * sizeof(float)));
+    carve_decode_ws(a, cfg, workspace, W, batch);
     cudaStream_t st = (cudaStream_t)stream;
     const bool tc = use_tc(cfg, batch) && al16(q_lat) && al16(q_pe) && al16(cache);
     a.tile = tc ? decode_tc_tile() : kTile;
@@ -263,7 +274,7 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
 int mla_decode_combine(const mla_config* cfg, const float* o_part, const float* lse_part,
                        int n_splits, int batch, void* o_lat, float* lse, mla_stream_t stream) {
     if (int rc = check_cfg(cfg)) return rc;
-    if (n_splits < 1 || n_splits > 1024 || batch < 1) return MLA_ERR_INVALID_ARG;
+    if (n_splits < 1 || n_splits > 512 || batch < 1) return MLA_ERR_INVALID_ARG;
     if (!o_part || !lse_part || !o_lat) return MLA_ERR_INVALID_ARG;
     return cuda_rc(launch_combine_dense(o_part, lse_part, n_splits, batch, cfg->heads,
                                         cfg->d_latent, o_lat, lse, cfg->dtype,
@@ -442,16 +453,13 @@ extern "C" int mla_decode_noalloc(const mla_config* cfg, const void* q_lat, cons
     if (int rc = status_ptr(&status)) return rc;
     // Nothing in the array has to start at zero: every partial slot the
     // merge reads is written earlier in the same call.
-    const size_t slots = (size_t)W + batch;
     DecodeArgs a{};
     a.heads = cfg->heads; a.d_latent = cfg->d_latent; a.d_rope = cfg->d_rope;
     a.block_size = cfg->block_size; a.max_blocks = max_blocks; a.batch = batch;
     a.workers = W; a.num_blocks = num_blocks; a.scale = cfg->softmax_scale;
     a.q_lat = q_lat; a.q_pe = q_pe; a.cache = cache; a.block_table = block_table;
     a.seq_lens = seq_lens; a.o_lat = o_lat; a.lse = lse; a.status = status;
-    a.o_part = (float*)scratch;
-    a.lse_part = (float*)((char*)scratch +
-                          align256(slots * cfg->heads * cfg->d_latent * sizeof(float)));
+    carve_decode_ws(a, cfg, scratch, W, batch);
     cudaStream_t st = (cudaStream_t)stream;
     const bool tc = use_tc(cfg, batch) && al16(q_lat) && al16(q_pe) && al16(cache);
     a.tile = tc ? decode_tc_tile() : kTile;

@@ -180,7 +180,7 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
  * Merges partial decode results computed over disjoint token ranges of the
  * same sequences (e.g. ranges held by different devices):
  *   LSE = log sum_s exp(lse_s),  o = sum_s exp(lse_s - LSE) o_s.
- *   o_part    [n_splits][batch][heads][d_latent] float32
+ *   o_part    [n_splits][batch][heads][d_latent] float32, 1 <= n_splits <= 512
  *   lse_part  [n_splits][batch][heads] float32; -inf marks an empty range
  *   o_lat     [batch][heads][d_latent] (written, dtype); all-empty rows give 0
  *   lse       [batch][heads] float32 or NULL (written)
@@ -232,8 +232,8 @@ int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, co
  * Arguments and results are those of mla_decode.  The call allocates nothing
  * (no cudaMalloc, cudaFree or allocating library routine).
  *   - Limit: the array must hold the partials of at least one worker plus one
- *     per sequence: (1 + batch) * heads * (d_latent + 1) * 4 bytes, rounded
- *     up to 256-byte regions.  Larger requests return MLA_ERR_UNSUPPORTED and
+ *     per sequence, (1 + batch) * heads * (d_latent + 1) * 4 bytes, and 16
+ *     bytes per sequence, each part rounded up to 256 bytes.  Larger requests return MLA_ERR_UNSUPPORTED and
  *     launch nothing.  When the array is smaller than what mla_decode would
  *     use, the context is split into fewer ranges (same result up to rounding).
  *   - The first call on a device looks up the array's device address with
