@@ -138,6 +138,26 @@ def test_append_indexing_is_bit_exact():
         assert rel(dense.float().cpu().numpy(), ref) <= tol
 
 
+def test_growing_scores_take_the_rescale_path():
+    """Cache rows scaled up page by page make every few tiles' score maximum
+    exceed the running one by more than the lazy-rescale threshold, so the
+    kernels rescale their accumulators several times per sequence; the result
+    must still match the oracle everywhere."""
+    lens = [1000, 600]
+    w = W.cached_decode(len(lens), lens, seed=12, permute=True)
+    bt = w["block_table"]
+    cache = w["cache"].float()
+    for b, n in enumerate(lens):
+        for j in range((n + 63) // 64):
+            cache[bt[b, j]] *= 1.0 + 1.5 * j
+    w["cache"] = cache.to(w["cache"].dtype)
+    step = run_step(w)
+    ref = O.reference_cached_decode(W.oracle_view(w))
+    res = step.results()
+    for key in ("o_lat", "o_v", "lse"):
+        assert rel(host(res[key]), ref[key]) <= TOL["bf16"], key
+
+
 def test_invalid_block_id_is_flagged_not_read():
     w = W.cached_decode(2, [100, 100], seed=8)
     w["block_table"][1, 1] = 10 ** 6
