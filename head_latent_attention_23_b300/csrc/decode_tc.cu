@@ -14,8 +14,11 @@
 // bf16, 144 KB) is too large to sit next to any part of O.  A 2-CTA cluster
 // therefore splits the work by kind, not by columns:
 //   - the score CTA (rank 0) keeps the latent part of Q in TMEM (256 columns,
-//     brought in by TMA and tcgen05.cp at the start of each sequence's range;
-//     the rotary part sits in shared memory) and computes S = Q C^T for
+//     brought in by TMA and tcgen05.cp at the start of each sequence's range,
+//     through the chunk ring except, on a worker's first range, the last two
+//     groups, which use the idle P staging slot so the first cache chunk
+//     starts loading with the query; the rotary part sits in shared memory)
+//     and computes S = Q C^T for
 //     128-token tiles (M=128, N=128, K=576: 36 MMAs) into two alternating
 //     128-column TMEM buffers, so S(k) runs while S(k-1) is read; its softmax
 //     warps turn S into bf16 P, stage P in
@@ -88,6 +91,8 @@ constexpr int kMaxBatch = 1024;
 constexpr int kMsgOff = kRingBytes;
 constexpr int kQpeOff = kMsgOff + kMsgBytes;
 static_assert(2 * kQpeBytes <= kMsgBytes, "rotary query buffers");
+static_assert((kQGroups - 2 * kSGroups) * kGroup <= kMsgBytes, "staged query chunk");
+static_assert(kQChunks == 3 && kQGroups - 2 * kSGroups == 2, "query chunking");
 constexpr int kBarOff = kMsgOff + kMsgSlots * kMsgBytes;
 constexpr int kRedOff = kBarOff + 512;     // softmax exchange: [4][128] fp32
 constexpr int kPreOff = kRedOff + 4 * 128 * 4;
@@ -116,6 +121,7 @@ struct Bars {
     uint64_t cfull[4], cempty[4];           // chunk ring
     uint64_t s_full[2], s_empty[2];         // score CTA: S double buffer
     uint64_t qpe_full[2], qpe_free[2];      // score CTA: rotary query of a range
+    uint64_t qs_full;                       // score CTA: first range's last query chunk
     uint64_t p_empty[kMsgSlots];            // score CTA: value CTA freed a message slot
     uint64_t p_full[kMsgSlots];             // value CTA: message landed
     uint64_t pv_done[kMsgSlots];            // value CTA: PV of the slot's tile finished
@@ -203,6 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap t_page,
                      const __grid_constant__ CUtensorMap t_qlat,
                      const __grid_constant__ CUtensorMap t_qpe,
+                     const __grid_constant__ CUtensorMap t_qlat2,
                      const __grid_constant__ DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -239,6 +246,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&bars->resc_done, 256);
         mbar_init(&bars->o_free, 256);
         mbar_init(&bars->mma_done, 1);
+        mbar_init(&bars->qs_full, 1);
         mbar_init(&bars->wg, 256);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -247,6 +255,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prefetch_tmap(&t_page);
         prefetch_tmap(&t_qlat);
         prefetch_tmap(&t_qpe);
+        prefetch_tmap(&t_qlat2);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_slot, kTmemCols);
@@ -272,7 +281,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             Cursor cur;
             cur.init(pre, a.batch, lo);
             int c = 0, seg = 0;
-            bool ok = true;
+            bool ok = true, staged = false;
+            const uint64_t evict_first = policy_evict_first();
             auto ring_slot = [&](int slots, int bytes) -> int {
                 const int s = c % slots;
                 if (!mbar_wait_fast(&bars->cempty[s], ((c / slots) & 1) ^ 1, abort_flag,
@@ -298,14 +308,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(&bars->qpe_full[qb], kQpeBytes);
                         tma_load_2d(smem + kQpeOff + qb * kQpeBytes, &t_qpe, 0, cur.b * kHeads,
                                     &bars->qpe_full[qb]);
+                        // the first range's last query chunk (two groups) goes to
+                        // the P staging slot, idle until the first P, so that the
+                        // tile's first cache chunk takes its ring slot at once
+                        const bool stage_q = seg == 0;
                         ++seg;
-                        for (int j = 0; j < kQChunks && ok; ++j, ++c) {
+                        for (int j = 0; j < kQChunks && ok; ++j) {
+                            if (stage_q && j == kQChunks - 1) {
+                                mbar_arrive_expect_tx(&bars->qs_full, 2 * kGroup);
+                                tma_load_3d(msg, &t_qlat2, 0, cur.b * kHeads, kSGroups * j,
+                                            &bars->qs_full);
+                                staged = true;
+                                continue;
+                            }
                             // three groups per box; the last box's third group
                             // lies past the query row and is zero-filled
                             const int s = ring_slot(kSSlots, kSChunk);
                             if (s < 0) break;
                             tma_load_3d(ring + s * kSChunk, &t_qlat, 0, cur.b * kHeads,
                                         kSGroups * j, &bars->cfull[s]);
+                            ++c;
                         }
                         if (!ok) break;
                     }
@@ -330,17 +352,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
-                    // the first tile's P arrives a full S and softmax after the
-                    // start: holding these loads back until then leaves the
-                    // score CTAs' first (cold) loads a less crowded memory system
-                    if (k == 0 && !mbar_wait_fast<true>(&bars->p_full[0], 0, abort_flag, a.status))
-                        break;
-                    // one box per chunk: 64 rows of a page x four 64-column groups
+                    // one box per chunk: 64 rows of a page x four 64-column
+                    // groups.  This is the last read of these rows: their L2
+                    // lines go first, ahead of the partials, queries and weights
+                    // that are read again
                     for (int j = 0; j < kVChunks && ok; ++j, ++c) {
                         const int s = ring_slot(kVSlots, kVChunk);
                         if (s < 0) break;
-                        tma_load_3d(ring + s * kVChunk, &t_page, 0, tr.row[j & 1], 4 * (j >> 1),
-                                    &bars->cfull[s]);
+                        tma_load_3d_hint(ring + s * kVChunk, &t_page, 0, tr.row[j & 1],
+                                         4 * (j >> 1), &bars->cfull[s], evict_first);
                     }
                 }
             }
@@ -351,6 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (scorer)
                 for (int i = seg > 2 ? seg - 2 : 0; i < seg; ++i)
                     drain_wait(&bars->qpe_full[i & 1], (i >> 1) & 1);
+            if (staged) drain_wait(&bars->qs_full, 0);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -365,16 +386,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < K && ok; ++k, cur.next()) {
                     if (cur.first(lo)) {
                         // new range: its latent query chunks into TMEM (in order
-                        // after the previous range's products), then its rotary part
-                        for (int j = 0; j < kQChunks; ++j, ++c) {
+                        // after the previous range's products), then its rotary
+                        // part; the first range's last chunk comes from the
+                        // staging slot (the softmax warps write P there only
+                        // after S(0), whose commit covers this copy)
+                        const bool staged = seg == 0;
+                        for (int j = 0; j < kQChunks; ++j) {
+                            const bool from_staging = staged && j == kQChunks - 1;
                             const int s = c % kSSlots;
-                            if (!mbar_wait_fast(&bars->cfull[s], (c / kSSlots) & 1, abort_flag,
-                                                a.status)) {
+                            uint64_t* full = from_staging ? &bars->qs_full : &bars->cfull[s];
+                            const uint32_t par = from_staging ? 0u : (uint32_t)((c / kSSlots) & 1);
+                            if (!mbar_wait_fast(full, par, abort_flag, a.status)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t st = smem_u32(ring + s * kSChunk);
+                            const uint32_t st = smem_u32(from_staging ? msg : ring + s * kSChunk);
                             for (int gg = 0; gg < kSGroups; ++gg) {
                                 const int qg = kSGroups * j + gg;
                                 if (qg >= kQGroups) break;
@@ -383,7 +410,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     tmem_cp_128x256b(tmem + kColQ + 32 * qg + 8 * kk,
                                                      sdesc(st + gg * kGroup + 32 * kk, 16, 1024, 2));
                             }
-                            tc_commit(&bars->cempty[s]);
+                            if (!from_staging) {
+                                tc_commit(&bars->cempty[s]);
+                                ++c;
+                            }
                         }
                         if (!ok) break;
                         qb = seg & 1;
@@ -815,7 +845,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
         return cudaErrorInvalidValue;
     DeviceState* d = device_state();
     if (!d || !d->attr) return cudaErrorNotSupported;
-    CUtensorMap t_cache, t_chunk, t_page, t_qlat, t_qpe;
+    CUtensorMap t_cache, t_chunk, t_page, t_qlat, t_qpe, t_qlat2;
     const uint64_t rows = (uint64_t)a.num_blocks * a.block_size;
     // cache rows, 64 x 64 boxes
     const uint64_t dims[2] = {(uint64_t)kD, rows};
@@ -833,13 +863,15 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
     const uint64_t dq[3] = {64, qrows, (uint64_t)kQGroups};
     const uint64_t sq[2] = {(uint64_t)kDL * 2, 128};
     const uint32_t bq3[3] = {64, kHeads, kSGroups};
+    const uint32_t bq2[3] = {64, kHeads, kQGroups - 2 * kSGroups};   // last two groups
     const uint64_t dp[2] = {(uint64_t)kDR, qrows}, sp[1] = {(uint64_t)kDR * 2};
     const uint32_t bq[2] = {64, kHeads};
     if (!make_tmap_bf16(&t_cache, a.cache, 2, dims, strides, box, 128) ||
         !make_tmap_bf16(&t_chunk, a.cache, 3, dims3, strides3, boxc, 128) ||
         !make_tmap_bf16(&t_page, a.cache, 3, dims3, strides3, box3, 128) ||
         !make_tmap_bf16(&t_qlat, a.q_lat, 3, dq, sq, bq3, 128) ||
-        !make_tmap_bf16(&t_qpe, a.q_pe, 2, dp, sp, bq, 128))
+        !make_tmap_bf16(&t_qpe, a.q_pe, 2, dp, sp, bq, 128) ||
+        !make_tmap_bf16(&t_qlat2, a.q_lat, 3, dq, sq, bq2, 128))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * a.workers);
@@ -852,7 +884,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_tc_kernel, t_cache, t_chunk, t_page, t_qlat, t_qpe,
-                              a);
+                              t_qlat2, a);
 }
 
 }  // namespace mla

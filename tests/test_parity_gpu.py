@@ -139,17 +139,20 @@ def test_append_indexing_is_bit_exact():
 
 
 def test_growing_scores_take_the_rescale_path():
-    """Cache rows scaled up page by page make every few tiles' score maximum
-    exceed the running one by more than the lazy-rescale threshold, so the
-    kernels rescale their accumulators several times per sequence; the result
-    must still match the oracle everywhere."""
+    """Cache rows scaled up geometrically page by page make the score maximum
+    of later tiles exceed the running one by more than the lazy-rescale
+    threshold (2^8), so the kernels rescale their accumulators many times in
+    the 1000-token sequence (about 80 head-tile events; logits reach ~11);
+    the result must still match the oracle everywhere.  The growth is kept
+    this mild on purpose: at logits near 60 the bf16 rounding of the absorbed
+    query alone moves the softmax by more than the bf16 tolerance."""
     lens = [1000, 600]
     w = W.cached_decode(len(lens), lens, seed=12, permute=True)
     bt = w["block_table"]
     cache = w["cache"].float()
     for b, n in enumerate(lens):
         for j in range((n + 63) // 64):
-            cache[bt[b, j]] *= 1.0 + 1.5 * j
+            cache[bt[b, j]] *= 0.03 * 1.35 ** j
     w["cache"] = cache.to(w["cache"].dtype)
     step = run_step(w)
     ref = O.reference_cached_decode(W.oracle_view(w))
