@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kWarps = 8;        // one head per warp
 constexpr int kMaxSlots = 512;
+constexpr int kEarly = 6;        // planned merges of up to 6 partials load every row at once
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -41,7 +42,7 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float 
 }
 
 template <typename T, bool kPlanned>
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(
+__global__ void __launch_bounds__(kWarps * 32, 2) combine_kernel(
     const float* __restrict__ o_part, const float* __restrict__ lse_part, int n_splits,
     int batch, int heads, int DL, T* __restrict__ o_lat, float* __restrict__ lse,
     const int4* __restrict__ seq_slots, int W) {
@@ -83,6 +84,25 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(
                         : o_part + (((size_t)slots[s] * batch + b) * heads + h) * DL;
     };
 
+    // A planned slot always holds a partial the decode kernel wrote, so with at
+    // most kEarly slots every row load is issued before the weights are known:
+    // the rows and the log-sum-exps then arrive in one memory round trip.
+    const bool early = kPlanned && ns <= kEarly && (DL & 3) == 0 && DL <= 512;
+    const int nq = (DL + 127) / 128;
+    float4 v8[kEarly][4];
+    if (early) {
+#pragma unroll
+        for (int i = 0; i < kEarly; ++i) {
+            const float* row = i < ns ? row_at(i) : nullptr;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = 4 * lane + 128 * q;
+                v8[i][q] = (row && q < nq && j < DL) ? *(const float4*)(row + j)
+                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+
     // weights: max and sum over the slots, 32 at a time
     float m = -INFINITY;
     for (int s = lane; s < ns; s += 32) m = fmaxf(m, lse_at(s));
@@ -99,11 +119,30 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(
     __syncwarp();
 
     T* out = o_lat + ((size_t)b * heads + h) * DL;
-    if ((DL & 3) == 0 && DL <= 512) {
+    if (early) {
+        float4 acc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < kEarly; ++i) {
+            const float w = i < ns ? wts[warp][i] * inv : 0.f;   // 0 for slot -1
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[q].x = fmaf(w, v8[i][q].x, acc[q].x);
+                acc[q].y = fmaf(w, v8[i][q].y, acc[q].y);
+                acc[q].z = fmaf(w, v8[i][q].z, acc[q].z);
+                acc[q].w = fmaf(w, v8[i][q].w, acc[q].w);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = 4 * lane + 128 * q;
+            if (q < nq && j < DL) store4<T>(out + j, acc[q].x, acc[q].y, acc[q].z, acc[q].w);
+        }
+    } else if ((DL & 3) == 0 && DL <= 512) {
         // lane: columns 4 * lane + 128 * q, q < DL / 128 (at most 4 float4).
         // Four partials at a time, every load of a batch issued before the
         // first multiply, so a warp waits for memory once per batch.
-        const int nq = (DL + 127) / 128;
         float4 acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
