@@ -62,6 +62,22 @@ def dist_env():
     return ws, rank, local
 
 
+def job_rate(local_ms, local_units, device="cpu"):
+    """Whole-job rate of a weak-scaling run: the units every rank processed,
+    summed, over the slowest rank's time (ms).  Returns (units per second,
+    slowest ms).  With one process (or no process group) it is the local rate.
+    `device` is where the reduction's tensors live: the rank's GPU under NCCL,
+    the CPU under gloo."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+        u = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+        local_ms, local_units = float(t.item()), float(u.item())
+    return local_units / (local_ms / 1e3), local_ms
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -350,23 +366,23 @@ def run_ours(args):
         torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    total_ms = start.elapsed_time(end)
+    # tokens of all ranks over the slowest rank's time
+    value, total_ms = job_rate(start.elapsed_time(end), B * K, dev)
     # the last replay of graph A: one duration per mla_decode call
     dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     assert mla.get_status() == mla.MLA_OK, "device status after timed region"
 
     # end to end: pinned host inputs -> device, step, result -> host
+    if ws > 1:
+        dist.barrier()
     e2e = run_e2e(steps[0], w, dev, stream, max(20, min(K, 2000)))
 
     if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
         return
     pk = peaks()
     ms_step = total_ms / K
-    value = ws * B * K / (total_ms / 1e3)
     dec_mean_ms = statistics.mean(dec_ms)
     dec_med_ms = statistics.median(dec_ms)
     hbm_gbs = cbytes / (dec_mean_ms * 1e-3) / 1e9
@@ -490,8 +506,9 @@ def run_e2e(s, w, dev, stream, K):
         host_out.copy_(result, non_blocking=True)
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / K
-    return {"value": w["batch"] / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    value, total = job_rate(a.elapsed_time(b), w["batch"] * K, dev)
+    ms = total / K
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K,
             "note": "same input set every step (L2-warm weights and cache)"}
 
