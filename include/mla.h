@@ -58,7 +58,7 @@ typedef struct CUstream_st* mla_stream_t; /* same object as cudaStream_t */
 typedef enum mla_status {
     MLA_OK = 0,
     MLA_ERR_INVALID_ARG = 1, /* bad pointer, size, or configuration value        */
-    MLA_ERR_UNSUPPORTED = 2, /* valid, but a shape/dtype this build cannot run   */
+    MLA_ERR_UNSUPPORTED = 2, /* valid, but a shape/dtype the library cannot run  */
     MLA_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small       */
     MLA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed             */
     MLA_ERR_TIMEOUT = 5,     /* device: a bounded wait in a kernel gave up       */
