@@ -90,6 +90,22 @@ def cached_decode(batch, seq_lens, seed=0, dtype="bf16", block_size=64, permute=
                 w_uk=w_uk, w_uv=w_uv, batch=batch)
 
 
+def growing_scores_decode(seed=12):
+    """Shared-cache decode (lengths 1000 and 600, pages permuted) whose cache
+    page j of each sequence is scaled by 0.03 * 1.35^j after drawing, so the
+    scores' maximum keeps rising along a sequence and an online softmax has to
+    move its running maximum many times."""
+    lens = [1000, 600]
+    w = cached_decode(len(lens), lens, seed=seed, permute=True)
+    bt = w["block_table"]
+    cache = w["cache"].float()
+    for b, n in enumerate(lens):
+        for j in range((n + 63) // 64):
+            cache[bt[b, j]] *= 0.03 * 1.35 ** j
+    w["cache"] = cache.to(w["cache"].dtype)
+    return w
+
+
 def token_decode(batch, ctx, seed=0, dtype="bf16", block_size=64, permute=False,
                  heads=128, d_latent=512, d_rope=64, d_nope=128, d_v=128, d_model=7168,
                  d_lq=1536, prior_rows="random"):

@@ -146,14 +146,7 @@ def test_growing_scores_take_the_rescale_path():
     the result must still match the oracle everywhere.  The growth is kept
     this mild on purpose: at logits near 60 the bf16 rounding of the absorbed
     query alone moves the softmax by more than the bf16 tolerance."""
-    lens = [1000, 600]
-    w = W.cached_decode(len(lens), lens, seed=12, permute=True)
-    bt = w["block_table"]
-    cache = w["cache"].float()
-    for b, n in enumerate(lens):
-        for j in range((n + 63) // 64):
-            cache[bt[b, j]] *= 0.03 * 1.35 ** j
-    w["cache"] = cache.to(w["cache"].dtype)
+    w = W.growing_scores_decode()      # premise checked on the CPU in test_workloads.py
     step = run_step(w)
     ref = O.reference_cached_decode(W.oracle_view(w))
     res = step.results()

@@ -29,3 +29,30 @@ def test_named_workload_shapes():
     assert w["x_new"].shape == (128, 256) and w["w_uq"].shape == (256, 8, 48)
     v = W.oracle_view(W.cached_decode(1, [3], heads=4, d_latent=8, d_rope=4, d_nope=4, d_v=4))
     assert v["cache"].dtype == np.uint16
+
+
+def test_growing_scores_inputs_cross_the_rescale_threshold_with_moderate_logits():
+    """Premise of the GPU rescale test: along sequence 0 the maximum of a
+    128-token tile's scores exceeds the running maximum by more than 8 (log2
+    units, the kernels' lazy-rescale threshold) many times over the heads,
+    while every logit stays below 15, where the bf16 tolerance holds."""
+    w = W.growing_scores_decode()
+    cfg = w["cfg"]
+    dl, D = cfg["d_latent"], cfg["d_latent"] + cfg["d_rope"]
+    n = int(w["seq_lens"][0])
+    tok = torch.arange(n)
+    slot = w["block_table"][0].long()[tok // 64] * 64 + tok % 64
+    rows = w["cache"].reshape(-1, D)[slot].double()
+    q_lat = torch.einsum("hn,hln->hl", w["q_nope"][0].double(), w["w_uk"].double())
+    s = cfg["softmax_scale"] * (q_lat @ rows[:, :dl].T + w["q_pe"][0].double() @ rows[:, dl:].T)
+    s2 = (s / np.log(2.0)).numpy()
+    events = 0
+    for h in range(s2.shape[0]):
+        m = -np.inf
+        for t0 in range(0, n, 128):
+            mt = s2[h, t0:t0 + 128].max()
+            if mt > m + 8.0:
+                events += m != -np.inf
+                m = mt
+    assert events >= 50, events
+    assert float(s.abs().max()) < 15.0
