@@ -24,6 +24,10 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(DecodeArgs a) {
     const int g = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int cap = a.max_blocks * a.block_size;
+    // This kernel is launched in plain stream order (no programmatic overlap),
+    // so the previous call's merge kernel has finished reading the workspace
+    // (or mla_decode_noalloc's shared static array) before anything here
+    // writes it.
     tile_prefix(a.seq_lens, a.batch, cap, pre, a.status);
     if (blockIdx.x == 0 && blockIdx.y == 0) publish_seq_slots(pre, a.batch, a.workers, a.seq_slots);
     const int64_t total = pre[a.batch];

@@ -27,6 +27,7 @@ struct DecodeArgs {
     void* o_lat;            // [batch][heads][d_latent]
     float* lse;             // [batch][heads] or null
     int* status;
+    uint64_t wait_ns;       // give-up time of the tensor-core kernel's pipeline waits
 };
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t st);

@@ -18,6 +18,10 @@ constexpr int kMaxDevices = 64;
 int* g_status_ptr[kMaxDevices];
 int g_num_sms[kMaxDevices];
 
+// Give-up time of the decode kernels' pipeline waits (mla_set_wait_limit_ns).
+constexpr uint64_t kDefaultWaitNs = 1000ull * 1000ull * 1000ull;
+uint64_t g_wait_ns = kDefaultWaitNs;
+
 int current_device(int* dev) {
     if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices)
         return MLA_ERR_CUDA;
@@ -144,6 +148,11 @@ const char* mla_status_string(int s) {
 
 int mla_version(void) { return 100; }
 
+int mla_set_wait_limit_ns(int64_t ns) {
+    g_wait_ns = ns > 0 ? (uint64_t)ns : kDefaultWaitNs;
+    return MLA_OK;
+}
+
 int mla_get_status(mla_stream_t stream, int* out) {
     if (!out) return MLA_ERR_INVALID_ARG;
     int* p;
@@ -262,6 +271,7 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
     a.workers = W; a.num_blocks = num_blocks; a.scale = cfg->softmax_scale;
     a.q_lat = q_lat; a.q_pe = q_pe; a.cache = cache; a.block_table = block_table;
     a.seq_lens = seq_lens; a.o_lat = o_lat; a.lse = lse; a.status = status;
+    a.wait_ns = g_wait_ns;
     carve_decode_ws(a, cfg, workspace, W, batch);
     cudaStream_t st = (cudaStream_t)stream;
     const bool tc = use_tc(cfg, batch) && al16(q_lat) && al16(q_pe) && al16(cache);
@@ -459,6 +469,7 @@ extern "C" int mla_decode_noalloc(const mla_config* cfg, const void* q_lat, cons
     a.workers = W; a.num_blocks = num_blocks; a.scale = cfg->softmax_scale;
     a.q_lat = q_lat; a.q_pe = q_pe; a.cache = cache; a.block_table = block_table;
     a.seq_lens = seq_lens; a.o_lat = o_lat; a.lse = lse; a.status = status;
+    a.wait_ns = g_wait_ns;
     carve_decode_ws(a, cfg, scratch, W, batch);
     cudaStream_t st = (cudaStream_t)stream;
     const bool tc = use_tc(cfg, batch) && al16(q_lat) && al16(q_pe) && al16(cache);

@@ -103,18 +103,22 @@ __device__ __forceinline__ bool mbar_poll_cluster(uint32_t addr, uint32_t parity
 }
 
 // Bounded wait without suspend hints, for the per-tile handshakes of the
-// decode pipeline.  Same give-up rule as mbar_wait.
+// decode pipeline.  Same give-up rule as mbar_wait, after `limit_ns`
+// (kWaitLimitNs unless a caller lowers it; a limit under 100 us is checked
+// after every poll so that it trips reliably).
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity,
-                                               volatile int* abort, int* status) {
+                                               volatile int* abort, int* status,
+                                               uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
     if (kCluster ? mbar_poll_cluster(a, parity) : mbar_poll(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint32_t every = limit_ns < 100000ull ? 0u : 63u;
     for (uint32_t i = 1;; ++i) {
         if (kCluster ? mbar_poll_cluster(a, parity) : mbar_poll(a, parity)) return true;
-        if ((i & 63u) == 0) {
+        if ((i & every) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 flag(status, MLA_ERR_TIMEOUT);
                 return false;

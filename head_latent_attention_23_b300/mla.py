@@ -31,7 +31,7 @@ EXPORTS = (
     "mla_status_string", "mla_version", "mla_decode_path", "mla_get_status",
     "mla_append_latent", "mla_absorb_q", "mla_decode_workspace_size", "mla_decode",
     "mla_decode_combine", "mla_project_out", "mla_query_proj_workspace_size", "mla_query_proj",
-    "mla_decode_noalloc",
+    "mla_decode_noalloc", "mla_set_wait_limit_ns",
 )
 
 
@@ -95,6 +95,7 @@ def lib():
         L.mla_query_proj_workspace_size.argtypes = [CP, I, I, SZ]
         L.mla_query_proj.argtypes = [CP, P, I, I, P, I, P, P, P, P, P, ctypes.c_size_t, P]
         L.mla_decode_noalloc.argtypes = [CP, P, P, P, I64, P, I, P, I, P, P, P]
+        L.mla_set_wait_limit_ns.argtypes = [I64]
         for name in EXPORTS:
             if name not in ("mla_status_string", "mla_version"):
                 getattr(L, name).restype = I
@@ -131,6 +132,12 @@ def _ptr(t, dtype=None, name="tensor"):
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def set_wait_limit_ns(ns):
+    """mla_set_wait_limit_ns: give-up time of the decode kernel's pipeline
+    waits for later calls (ns <= 0: the default, 1 s).  For tests."""
+    _check(lib().mla_set_wait_limit_ns(int(ns)), "mla_set_wait_limit_ns")
 
 
 def decode_path(cfg):

@@ -106,6 +106,51 @@ def growing_scores_decode(seed=12):
     return w
 
 
+def growing_scores_exact_query_decode(seed=12):
+    """Shared-cache decode (lengths 1000 and 600, pages permuted) built so
+    that the scores grow to logits of about 58 while the absorbed query stays
+    exactly representable in bf16.
+
+    Draw order: that of cached_decode(seed), then one index j(b, h) in
+    [0, d_nope) per (sequence, head).  q_nope[b, h] is replaced by the unit
+    vector e_j, so q_lat[b, h] = q_nope[b, h] . W_LK_h^T is column j of
+    W_LK_h: a single product with 1.0, exact in any precision.  Cache page j
+    of each sequence is then scaled by 1 + 1.5 j, so the running maximum of
+    the scores keeps rising along a sequence (hundreds of head-tile events
+    above the 2^8 lazy-rescale threshold of the tensor-core kernel)."""
+    lens = [1000, 600]
+    w = cached_decode(len(lens), lens, seed=seed, permute=True)
+    g = torch.Generator().manual_seed(seed + 1)
+    B, H, dn = w["q_nope"].shape
+    idx = torch.randint(0, dn, (B, H), generator=g)
+    q = torch.zeros(B, H, dn)
+    q.scatter_(2, idx[..., None], 1.0)
+    w["q_nope"] = q.to(w["q_nope"].dtype)
+    bt = w["block_table"]
+    cache = w["cache"].float()
+    for b, n in enumerate(lens):
+        for j in range((n + 63) // 64):
+            cache[bt[b, j]] *= 1.0 + 1.5 * j
+    w["cache"] = cache.to(w["cache"].dtype)
+    return w
+
+
+def crossing_ranges_decode(seed=31, batch=80, d_nope=64, d_v=8):
+    """Shared-cache decode with many short and medium sequences (lengths
+    uniform in [1, 700], one sequence of 37 tokens in the middle of the
+    batch, pages permuted), so that a split of the context into equal tile
+    ranges puts several sequence boundaries inside most ranges.  DeepSeek-V2
+    head, latent and rotary widths; d_nope and d_v are smaller than
+    DeepSeek's only to keep the unmerged CPU reference fast (the attention
+    core sees the absorbed query and does not depend on them).
+
+    Draw order: lengths, then that of cached_decode(seed)."""
+    g = torch.Generator().manual_seed(seed + 104729)
+    lens = torch.randint(1, 701, (batch,), generator=g).tolist()
+    lens[batch // 2] = 37
+    return cached_decode(batch, lens, seed=seed, permute=True, d_nope=d_nope, d_v=d_v)
+
+
 def token_decode(batch, ctx, seed=0, dtype="bf16", block_size=64, permute=False,
                  heads=128, d_latent=512, d_rope=64, d_nope=128, d_v=128, d_model=7168,
                  d_lq=1536, prior_rows="random"):

@@ -107,6 +107,18 @@ int mla_version(void);
 int mla_decode_path(const mla_config* cfg);
 
 /*
+ * Diagnostic: how long a pipeline wait inside the tensor-core decode kernel
+ * may last before the kernel gives up (default 1 s; ns <= 0 restores it).
+ * A kernel that gives up records MLA_ERR_TIMEOUT in the status word, lets
+ * its copies land, waits for its tensor-core operations, frees its tensor
+ * memory and returns, so the next call on the device runs normally.  The
+ * value applies to decode calls issued afterwards from any thread.  It exists
+ * so that tests can make the give-up path run; the pages describe nothing
+ * like it.  Always returns MLA_OK.
+ */
+int mla_set_wait_limit_ns(int64_t ns);
+
+/*
  * Reads and clears the current device's status word (see above).  Waits for
  * `stream` to finish first.  *out receives MLA_OK or the first device-side
  * error recorded since the last call.

@@ -56,3 +56,81 @@ def test_growing_scores_inputs_cross_the_rescale_threshold_with_moderate_logits(
                 m = mt
     assert events >= 50, events
     assert float(s.abs().max()) < 15.0
+
+
+def _scores(w, b):
+    """fp64 scaled scores [heads, n] of sequence b in the absorbed form."""
+    cfg = w["cfg"]
+    dl, D = cfg["d_latent"], cfg["d_latent"] + cfg["d_rope"]
+    n = int(w["seq_lens"][b])
+    tok = torch.arange(n)
+    slot = w["block_table"][b].long()[tok // 64] * 64 + tok % 64
+    rows = w["cache"].reshape(-1, D)[slot].double()
+    q_lat = torch.einsum("hn,hln->hl", w["q_nope"][b].double(), w["w_uk"].double())
+    s = cfg["softmax_scale"] * (q_lat @ rows[:, :dl].T + w["q_pe"][b].double() @ rows[:, dl:].T)
+    return s, q_lat, rows
+
+
+def _rescale_events(s):
+    s2 = (s / np.log(2.0)).numpy()
+    events = 0
+    for h in range(s2.shape[0]):
+        m = -np.inf
+        for t0 in range(0, s2.shape[1], 128):
+            mt = s2[h, t0:t0 + 128].max()
+            if mt > m + 8.0:
+                events += m != -np.inf
+                m = mt
+    return events
+
+
+def test_exact_query_inputs_reach_large_logits_with_many_rescales():
+    """Premise of the GPU large-logit test: the absorbed query is exact in
+    bf16 (one-hot q_nope picks one column of W_LK_h), the logits reach 50 and
+    more, and the 2^8 lazy-rescale threshold is crossed hundreds of times."""
+    w = W.growing_scores_exact_query_decode()
+    s, q_lat, _ = _scores(w, 0)
+    assert torch.equal(q_lat.to(torch.bfloat16).double(), q_lat)
+    assert float(s.max()) > 50.0
+    assert _rescale_events(s) >= 200
+
+
+def test_bf16_rounding_of_a_general_absorbed_query_moves_large_logit_outputs():
+    """Why the large-logit GPU test uses an exact query: with an ordinary
+    q_nope, rounding q_lat = q_nope . W_LK_h^T to bf16 (the decode call's input
+    type) moves o_lat by more than the 5e-3 bf16 bar once logits approach 60,
+    before any kernel arithmetic.  Absorbed-form fp64 attention with the
+    exact and with the rounded query, same cache as the exact-query test."""
+    w = W.growing_scores_exact_query_decode()
+    g = torch.Generator().manual_seed(5)
+    w["q_nope"] = torch.randn(w["q_nope"].shape, generator=g).to(torch.bfloat16)
+    s, q_lat, rows = _scores(w, 0)
+    cfg = w["cfg"]
+    dl = cfg["d_latent"]
+    qr = q_lat.to(torch.bfloat16).double()
+    q_pe = w["q_pe"][0].double()
+    s_r = cfg["softmax_scale"] * (qr @ rows[:, :dl].T + q_pe @ rows[:, dl:].T)
+    o = torch.softmax(s, dim=1) @ rows[:, :dl]
+    o_r = torch.softmax(s_r, dim=1) @ rows[:, :dl]
+    assert float(s.max()) > 40.0
+    assert float((o - o_r).abs().max() / o.abs().max()) > 5e-3
+
+
+def test_crossing_ranges_inputs_put_sequence_ends_inside_most_ranges():
+    """Premise of the GPU split-range test: with the context cut into equal
+    ranges of 128-token tiles over 74 workers (two SMs each on a 148-SM
+    B300), there are at least three tiles per worker and most workers' ranges
+    hold parts of two or more sequences."""
+    w = W.crossing_ranges_decode()
+    lens = w["seq_lens"].tolist()
+    pre = np.concatenate([[0], np.cumsum([(n + 127) // 128 for n in lens])])
+    total, workers = int(pre[-1]), 74
+    assert total >= 3 * workers
+    crossing = 0
+    for g in range(workers):
+        lo, hi = g * total // workers, (g + 1) * total // workers
+        first = np.searchsorted(pre, lo, side="right") - 1
+        last = np.searchsorted(pre, hi - 1, side="right") - 1
+        crossing += last > first
+    assert crossing >= workers // 2
+    assert 37 in lens and min(lens) >= 1

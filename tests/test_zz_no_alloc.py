@@ -60,6 +60,36 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row():
     assert _rel(o2, r2) <= TOL and _rel(l2, rl2) <= TOL
 
 
+def test_noalloc_with_fewer_split_ranges_than_decode_matches_decode():
+    """At batch 100 the partials of mla_decode's full split (one per worker
+    plus one per sequence) do not fit the array, so the no-allocation call
+    cuts the context into fewer ranges: same result up to rounding."""
+    g = torch.Generator().manual_seed(24)
+    lens = torch.randint(1, 601, (100,), generator=g).tolist()
+    cfg, t = _inputs(lens, seed=24)
+    (o, l), (r, rl) = _both(cfg, t)
+    assert _rel(o, r) <= TOL and _rel(l, rl) <= TOL
+
+
+def test_noalloc_batch_limit_is_126_at_deepseek_shapes():
+    """(1 + batch) slots of 128 heads x (512 + 1) fp32 plus 16 bytes per
+    sequence fit the 32 MiB array up to batch 126: that batch runs (one split
+    range) and matches mla_decode, batch 127 is refused."""
+    g = torch.Generator().manual_seed(25)
+    lens = torch.randint(1, 200, (126,), generator=g).tolist()
+    cfg, t = _inputs(lens, seed=25)
+    (o, l), (r, rl) = _both(cfg, t)
+    assert _rel(o, r) <= TOL and _rel(l, rl) <= TOL
+    B = 127
+    q_lat = torch.zeros(B, 128, 512, dtype=torch.bfloat16, device="cuda")
+    q_pe = torch.zeros(B, 128, 64, dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros(B, 1, dtype=torch.int32, device="cuda")
+    sl = torch.ones(B, dtype=torch.int32, device="cuda")
+    with pytest.raises(mla.MLAError) as e:
+        mla.decode_noalloc(cfg, q_lat, q_pe, t["cache"], bt, sl, torch.zeros_like(q_lat))
+    assert e.value.status == mla.MLA_ERR_UNSUPPORTED
+
+
 def test_noalloc_refuses_batches_beyond_its_array():
     cfg, t = _inputs([5], seed=23)
     # (1 + batch) partial slots of 128 heads x 512 fp32 no longer fit 32 MiB
