@@ -14,16 +14,15 @@
 // bf16, 144 KB) is too large to sit next to any part of O.  A 2-CTA cluster
 // therefore splits the work by kind, not by columns:
 //   - the score CTA (rank 0) keeps the latent part of Q in TMEM (256 columns,
-//     brought in by TMA and tcgen05.cp at the start of each sequence's range;
-//     the query chunks go through the same ring as the cache chunks,
-//     interleaved with the first tile's, so the first product starts as soon
-//     as its own query and cache columns have landed; the rotary part sits in
-//     shared memory) and computes S = Q C^T for 128-token tiles (M=128,
-//     N=128, K=576: 36 MMAs) into two alternating 128-column TMEM buffers, so
-//     S(k) runs while S(k-1) is read; its softmax warps turn S into bf16 P
-//     and store it, 16 bytes per instruction, straight into a receive slot of
-//     the value CTA (st.async, counted on the value CTA's barrier), already in
-//     the operand layout of the next product;
+//     brought in by TMA and tcgen05.cp at the start of each sequence's range,
+//     through the chunk ring except, on a worker's first range, the last two
+//     groups, which use the idle P staging slot so the first cache chunk
+//     starts loading with the query; the rotary part sits in shared memory)
+//     and computes S = Q C^T for 128-token tiles (M=128, N=128, K=576: 36
+//     MMAs) into two alternating 128-column TMEM buffers, so S(k) runs while
+//     S(k-1) is read; its softmax warps turn S into bf16 P, stage P in the
+//     operand layout of the next product and push it, 34 KB per tile, into
+//     the value CTA's shared memory with one bulk copy;
 //   - the value CTA (rank 1) keeps O in all 512 TMEM columns and computes
 //     O += P C (M=128, N=256, K=128: 16 MMAs) from its own copy of the tile's
 //     latent columns.
@@ -31,13 +30,21 @@
 // because a TMA box costs a roughly fixed time on top of its bytes: the score
 // CTA takes all 576 columns of a tile in three 48 KB chunks of three 64-column
 // groups x 128 tokens (one box of a 3-D [group][row][column] view of the cache
-// when the tile's two pages are adjacent in the pool, else 64-row boxes) into
-// a ring of four such chunks, so more than a tile's bytes are in flight; the
+// when the tile's two pages are adjacent in the pool, else 64-row boxes), the
 // value CTA takes the 512 latent columns in four (column half, page) chunks,
 // each one box of 64 rows x four 64-column groups of a 3-D view of the cache,
 // which hit L2 right after the score CTA brought them in.  Only P crosses the
 // cluster; distributed shared memory moves about 12 bytes per clock, so the
 // fp32 partial scores of a column split (64 KB per tile each way) would not fit.
+//
+// Issue paths.  One thread issues every MMA of a CTA and one every TMA copy,
+// and each SM sub-partition runs one of them next to two softmax or epilogue
+// warps.  Two things keep those threads fast: the MMA operand descriptors are
+// computed once per operand tile and advanced by constant adds (a descriptor
+// computed inline before each MMA makes the tensor pipe wait for the issuing
+// thread), and the hot loops are small (bounded waits keep their slow path
+// out of line, the softmax walks S in four 16-column pieces), because the
+// warps of a sub-partition share one small instruction cache.
 //
 // Softmax.  Thread h of the score CTA owns head h (TMEM lane h).  The running
 // max m only moves when a tile's max exceeds it by more than 2^8; the tile's
@@ -64,20 +71,21 @@ constexpr int kHeads = 128, kDL = 512, kDR = 64, kD = kDL + kDR;
 constexpr int kT = 128;                  // tokens per tile
 constexpr int kHalf = 64;                // rows per TMA box (a tile = two boxes)
 constexpr int kBox = kHalf * 64 * 2;     // 8 KB: 64 rows x 64 columns
-// score CTA ring: chunks of three 64-column groups x 128 rows (48 KB): a cache
-// tile is three chunks (576 columns = 9 groups), the latent query of a range
-// another three (the last holds two groups and a zero-filled third)
+// score CTA ring: chunks of three 64-column groups x 128 tokens (48 KB), three
+// chunks per tile (576 columns = 9 groups); a group's tile is 128 rows x 128 B
 constexpr int kGroup = 2 * kBox;             // 16 KB: one 64-column group, 128 rows
 constexpr int kSGroups = 3;                  // groups per chunk
 constexpr int kSChunk = kSGroups * kGroup;   // 48 KB
-constexpr int kSChunks = 3;                  // cache chunks per tile
-constexpr int kSSlots = 4;
+constexpr int kSChunks = 3;                  // chunks per tile
+constexpr int kSSlots = 3;
 // value CTA ring: 256 columns x 64 tokens per chunk, four chunks per tile
 constexpr int kVChunk = 4 * kBox;
 constexpr int kVChunks = 4;
 constexpr int kVSlots = 4;
+constexpr int kRingBytes = kSSlots * kSChunk;
+static_assert(kRingBytes >= kVSlots * kVChunk, "one ring region for both roles");
 // message: P [128 heads x 128 tokens] bf16 as two K-major 128-byte-swizzled
-// blocks of 64 tokens, then the aux block
+// blocks of 64 tokens, then the per-head factors
 constexpr int kPBytes = kHeads * kT * 2;   // 32 KB
 constexpr int kAuxBytes = 2048;    // factors, row sums, flags, valid rows
 constexpr int kMsgBytes = kPBytes + kAuxBytes;
@@ -86,39 +94,28 @@ constexpr int kQGroups = 8;              // latent query: eight 64-column groups
 constexpr int kQChunks = 3;              // ... in chunks of three groups (the last has two)
 constexpr int kQpeBytes = kHeads * kDR * 2;   // 16 KB
 constexpr int kMaxBatch = 1024;
-// Shared-memory layout.  Both CTAs run the same kernel; each uses its own
-// part of one layout:
-//   score CTA: [ring: 4 x 48 KB][rotary query 16 KB]
-//   value CTA: [ring: 4 x 32 KB][receive slot 0][receive slot 1]
-// then, for both: barriers, the softmax exchange, the tile prefix.
-constexpr int kSRing = kSSlots * kSChunk;
-constexpr int kVRing = kVSlots * kVChunk;
-constexpr int kQpeOff = kSRing;
-constexpr int kMsgOff = kVRing;
-constexpr int kRegion = kQpeOff + kQpeBytes > kMsgOff + kMsgSlots * kMsgBytes
-                            ? kQpeOff + kQpeBytes
-                            : kMsgOff + kMsgSlots * kMsgBytes;
-static_assert(kQChunks * kSGroups >= kQGroups, "query chunking");
-constexpr int kBarOff = kRegion;
-constexpr int kRedOff = kBarOff + 512;     // softmax exchange: [2][2][128] tile max, [2][128] sums
-constexpr int kRedBytes = 6 * 128 * 4;
-constexpr int kPreOff = kRedOff + kRedBytes;
+// The score CTA stages one outgoing message at kMsgOff and keeps the rotary
+// query of two consecutive ranges in the space of the second receive slot.
+constexpr int kMsgOff = kRingBytes;
+constexpr int kQpeOff = kMsgOff + kMsgBytes;
+static_assert(2 * kQpeBytes <= kMsgBytes, "rotary query buffers");
+static_assert((kQGroups - 2 * kSGroups) * kGroup <= kMsgBytes, "staged query chunk");
+static_assert(kQChunks == 3 && kQGroups - 2 * kSGroups == 2, "query chunking");
+constexpr int kBarOff = kMsgOff + kMsgSlots * kMsgBytes;
+constexpr int kRedOff = kBarOff + 512;     // softmax exchange: [4][128] fp32
+constexpr int kPreOff = kRedOff + 4 * 128 * 4;
 constexpr int kLenOff = kPreOff + (kMaxBatch + 1) * 4;
 constexpr int kSmemBytes = 1024 + kLenOff + kMaxBatch * 4;
 constexpr int kThreads = 320;      // producer, MMA, 8 softmax / epilogue warps
 static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kMsgBytes % 1024 == 0 && kMsgOff % 1024 == 0,
-              "receive slots keep the 1 KB swizzle alignment");
+static_assert(kMsgBytes % 1024 == 0, "message slots keep the 1 KB swizzle alignment");
 
 // aux block of a message (offsets in 4-byte words after P)
 constexpr int kAuxAlpha = 0;     // [128] factor applied to O rows before this tile
-constexpr int kAuxSum = 128;     // [2][128] row sums of the two token halves (read on the last tile)
+constexpr int kAuxSum = 128;     // [2][128] row sums of the two token halves (last tile)
 constexpr int kAuxFlags = 384;   // [4] per softmax warp: some row of it rescales
 constexpr int kAuxValid = 388;   // [2] valid rows of the two 64-token halves
 static_assert((kAuxValid + 2) * 4 <= kAuxBytes, "aux block");
-// bytes the score CTA stores into a receive slot per tile: P, 128 factors,
-// 256 row sums, 4 flags, 2 valid-row counts
-constexpr uint32_t kMsgSent = kPBytes + (128 + 256 + 4 + 2) * 4;
 
 // TMEM columns
 constexpr uint32_t kColQ = 0;      // score CTA: 256 columns, latent Q bf16 pairs [head][k]
@@ -128,11 +125,37 @@ constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
+// Optional timeline of a launch (built only with -DMLA_DECODE_TRACE): per CTA
+// and tile, %globaltimer stamps of pipeline events; per CTA, its start and end.
+#ifdef MLA_DECODE_TRACE
+constexpr int kTraceCtas = 256, kTraceTiles = 16, kTraceEvents = 8;
+__device__ unsigned long long g_decode_trace[kTraceCtas * kTraceTiles * kTraceEvents];
+__device__ unsigned long long g_decode_trace_cta[kTraceCtas * 4];
+#define DECODE_TRACE(ev, k)                                                              \
+    do {                                                                                 \
+        if ((k) < kTraceTiles && blockIdx.x < kTraceCtas)                                \
+            g_decode_trace[((size_t)blockIdx.x * kTraceTiles + (k)) * kTraceEvents + (ev)] = \
+                globaltimer_ns();                                                        \
+    } while (0)
+#define DECODE_TRACE_CTA(ev)                                                             \
+    do {                                                                                 \
+        if (blockIdx.x < kTraceCtas) g_decode_trace_cta[blockIdx.x * 4 + (ev)] = globaltimer_ns(); \
+    } while (0)
+#else
+#define DECODE_TRACE(ev, k) \
+    do {                    \
+    } while (0)
+#define DECODE_TRACE_CTA(ev) \
+    do {                     \
+    } while (0)
+#endif
+
 struct Bars {
     uint64_t cfull[4], cempty[4];           // chunk ring
     uint64_t s_full[2], s_empty[2];         // score CTA: S double buffer
-    uint64_t qpe_full, qpe_free;            // score CTA: rotary query of a range
-    uint64_t p_empty[kMsgSlots];            // score CTA: value CTA freed a receive slot
+    uint64_t qpe_full[2], qpe_free[2];      // score CTA: rotary query of a range
+    uint64_t qs_full;                       // score CTA: first range's last query chunk
+    uint64_t p_empty[kMsgSlots];            // score CTA: value CTA freed a message slot
     uint64_t p_full[kMsgSlots];             // value CTA: message landed
     uint64_t pv_done[kMsgSlots];            // value CTA: PV of the slot's tile finished
     uint64_t zeroed, resc_done, o_free, mma_done;
@@ -193,18 +216,60 @@ __device__ __forceinline__ TileRows tile_rows(const DecodeArgs& a, int b, int n,
     return r;
 }
 
+// MMA issue with precomputed operands.  A single thread issues every MMA of
+// a CTA, so the instructions between two MMAs are a dependent chain on the
+// issue path: descriptors are computed once per operand tile and advanced by
+// adding the k step (32 bytes = 2 in the descriptor's address field, which
+// cannot carry: shared addresses stay below 256 KB), and the accumulate flag
+// is an immediate wherever it is known at compile time.
+__device__ __forceinline__ void mma_ss_acc(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d), "l"(a), "l"(b),
+                 "r"(idesc)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_ts_acc(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d), "r"(a), "l"(b),
+                 "r"(idesc)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_ts_new(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d), "r"(a), "l"(b),
+                 "r"(idesc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                         uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most N bulk groups of this thread still read their source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap t_cache,
                      const __grid_constant__ CUtensorMap t_chunk,
                      const __grid_constant__ CUtensorMap t_page,
                      const __grid_constant__ CUtensorMap t_qlat,
                      const __grid_constant__ CUtensorMap t_qpe,
+                     const __grid_constant__ CUtensorMap t_qlat2,
                      const __grid_constant__ DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* ring = smem;
-    uint8_t* msg = smem + kMsgOff;          // value CTA: receive slots
-    uint8_t* qpe = smem + kQpeOff;          // score CTA: rotary query
+    uint8_t* msg = smem + kMsgOff;
     Bars* bars = (Bars*)(smem + kBarOff);
     int* pre = (int*)(smem + kPreOff);
     int* lens = (int*)(smem + kLenOff);
@@ -218,6 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int cap = a.max_blocks * a.block_size;
 
     if (threadIdx.x == 0) {
+        DECODE_TRACE_CTA(0);
         for (int s = 0; s < 4; ++s) {
             mbar_init(&bars->cfull[s], 1);
             mbar_init(&bars->cempty[s], 1);
@@ -225,18 +291,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->s_full[s], 1);
             mbar_init(&bars->s_empty[s], 256);
+            mbar_init(&bars->qpe_full[s], 1);
+            mbar_init(&bars->qpe_free[s], 1);
         }
-        mbar_init(&bars->qpe_full, 1);
-        mbar_init(&bars->qpe_free, 1);
         for (int s = 0; s < kMsgSlots; ++s) {
             mbar_init(&bars->p_empty[s], 8);     // one remote arrive per value-CTA warp
-            mbar_init(&bars->p_full[s], 1);      // local expect_tx + the peer's stores
+            mbar_init(&bars->p_full[s], 1);      // local expect_tx + the bulk copy
             mbar_init(&bars->pv_done[s], 1);
         }
         mbar_init(&bars->zeroed, 256);
         mbar_init(&bars->resc_done, 256);
         mbar_init(&bars->o_free, 256);
         mbar_init(&bars->mma_done, 1);
+        mbar_init(&bars->qs_full, 1);
         mbar_init(&bars->wg, 256);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -245,6 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prefetch_tmap(&t_page);
         prefetch_tmap(&t_qlat);
         prefetch_tmap(&t_qpe);
+        prefetch_tmap(&t_qlat2);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_slot, kTmemCols);
@@ -273,7 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             Cursor cur;
             cur.init(pre, a.batch, lo);
             int c = 0, seg = 0;
-            bool ok = true;
+            bool ok = true, staged = false;
             const uint64_t evict_first = policy_evict_first();
             auto ring_slot = [&](int slots, int bytes) -> int {
                 const int s = c % slots;
@@ -289,41 +357,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int t0 = cur.tile_in_seq() * kT;
                 const TileRows tr = tile_rows(a, cur.b, lens[cur.b], t0, scorer);
                 if (scorer) {
-                    const bool fst = cur.first(lo);
+                    if (cur.first(lo)) {
+                        // the range's query: the rotary part into its own buffer
+                        // (free once the previous use's products are done), the
+                        // latent part through the ring for tcgen05.cp into TMEM
+                        const int qb = seg & 1;
+                        if (!mbar_wait_fast(&bars->qpe_free[qb], ((seg >> 1) & 1) ^ 1,
+                                            abort_flag, a.status, wl))
+                            break;
+                        mbar_arrive_expect_tx(&bars->qpe_full[qb], kQpeBytes);
+                        tma_load_2d(smem + kQpeOff + qb * kQpeBytes, &t_qpe, 0, cur.b * kHeads,
+                                    &bars->qpe_full[qb]);
+                        // the first range's last query chunk (two groups) goes to
+                        // the P staging slot, idle until the first P, so that the
+                        // tile's first cache chunk takes its ring slot at once
+                        const bool stage_q = seg == 0;
+                        ++seg;
+                        for (int j = 0; j < kQChunks && ok; ++j) {
+                            if (stage_q && j == kQChunks - 1) {
+                                mbar_arrive_expect_tx(&bars->qs_full, 2 * kGroup);
+                                tma_load_3d(msg, &t_qlat2, 0, cur.b * kHeads, kSGroups * j,
+                                            &bars->qs_full);
+                                staged = true;
+                                continue;
+                            }
+                            // three groups per box; the last box's third group
+                            // lies past the query row and is zero-filled
+                            const int s = ring_slot(kSSlots, kSChunk);
+                            if (s < 0) break;
+                            tma_load_3d(ring + s * kSChunk, &t_qlat, 0, cur.b * kHeads,
+                                        kSGroups * j, &bars->cfull[s]);
+                            ++c;
+                        }
+                        if (!ok) break;
+                    }
                     // the two pages of the tile in one 128-row box when they are
                     // adjacent in the pool (fewer, larger TMA requests), else one
                     // 64-row box each; the shared-memory image is the same
                     const bool adjacent = tr.valid[1] > 0 && tr.row[1] == tr.row[0] + kHalf;
-                    // a range's first tile interleaves its latent query chunks
-                    // with its cache chunks: Q0 C0 Q1 C1 Q2 C2
-                    const int n = fst ? 2 * kSChunks : kSChunks;
-                    const int qpe_at = fst ? (seg == 0 ? 0 : 4) : -1;
-                    for (int i = 0; i < n && ok; ++i, ++c) {
-                        if (i == qpe_at) {
-                            // the range's rotary query, first needed by C2.  Its
-                            // buffer is free once the previous range's last
-                            // product is done, so on later ranges it is loaded
-                            // only after Q0 C0 Q1 C1 are on their way.
-                            if (!mbar_wait_fast(&bars->qpe_free, (seg & 1) ^ 1, abort_flag,
-                                                a.status, wl)) {
-                                ok = false;
-                                break;
-                            }
-                            mbar_arrive_expect_tx(&bars->qpe_full, kQpeBytes);
-                            tma_load_2d(qpe, &t_qpe, 0, cur.b * kHeads, &bars->qpe_full);
-                            ++seg;
-                        }
-                        const bool isq = fst && (i & 1) == 0;
-                        const int j = fst ? i >> 1 : i;
+                    for (int j = 0; j < kSChunks && ok; ++j, ++c) {
                         const int s = ring_slot(kSSlots, kSChunk);
                         if (s < 0) break;
                         uint8_t* dst = ring + s * kSChunk;
-                        if (isq) {
-                            // three query groups per box; the last box's third
-                            // group lies past the query row and is zero-filled
-                            tma_load_3d(dst, &t_qlat, 0, cur.b * kHeads, kSGroups * j,
-                                        &bars->cfull[s]);
-                        } else if (adjacent) {
+                        if (adjacent) {
                             tma_load_3d(dst, &t_chunk, 0, tr.row[0], kSGroups * j, &bars->cfull[s]);
                         } else {
                             for (int gg = 0; gg < kSGroups; ++gg) {
@@ -352,7 +428,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int slots = scorer ? kSSlots : kVSlots;
             for (int i = c > slots ? c - slots : 0; i < c; ++i)
                 drain_wait(&bars->cfull[i % slots], (i / slots) & 1);
-            if (seg > 0) drain_wait(&bars->qpe_full, (seg - 1) & 1);
+            if (scorer)
+                for (int i = seg > 2 ? seg - 2 : 0; i < seg; ++i)
+                    drain_wait(&bars->qpe_full[i & 1], (i >> 1) & 1);
+            if (staged) drain_wait(&bars->qs_full, 0);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -361,50 +440,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             cur.init(pre, a.batch, lo);
             bool ok = true;
             if (scorer) {
-                // S = Q C^T, K = 576 in nine 64-column groups of four k-steps
+                // S = Q C^T, K = 576 in nine 64-column chunks of four k-steps
                 const uint32_t id_s = idesc_bf16(128, kT, false, false);
-                const uint32_t qa = smem_u32(qpe);
-                int c = 0, seg = 0;
+                int c = 0, seg = 0, qb = 0;
                 for (int k = 0; k < K && ok; ++k, cur.next()) {
-                    const bool fst = cur.first(lo);
-                    const int sb = k & 1;   // S buffer: the softmax warps read S(k-1) meanwhile
-                    const uint32_t d_s = tmem + kColS + 128 * sb;
-                    const int n = fst ? 2 * kSChunks : kSChunks;
-                    bool s_free = false;
-                    for (int i = 0; i < n; ++i, ++c) {
-                        const bool isq = fst && (i & 1) == 0;
-                        const int j = fst ? i >> 1 : i;
-                        const int s = c % kSSlots;
-                        if (!isq && !s_free) {
-                            if (!mbar_wait_fast(&bars->s_empty[sb], ((k >> 1) & 1) ^ 1,
-                                                abort_flag, a.status, wl)) {
+                    if (cur.first(lo)) {
+                        // new range: its latent query chunks into TMEM (in order
+                        // after the previous range's products), then its rotary
+                        // part; the first range's last chunk comes from the
+                        // staging slot (the softmax warps write P there only
+                        // after S(0), whose commit covers this copy)
+                        const bool staged = seg == 0;
+                        for (int j = 0; j < kQChunks; ++j) {
+                            const bool from_staging = staged && j == kQChunks - 1;
+                            const int s = c % kSSlots;
+                            uint64_t* full = from_staging ? &bars->qs_full : &bars->cfull[s];
+                            const uint32_t par = from_staging ? 0u : (uint32_t)((c / kSSlots) & 1);
+                            if (!mbar_wait_fast(full, par, abort_flag, a.status, wl)) {
                                 ok = false;
                                 break;
                             }
-                            s_free = true;
-                        }
-                        if (!isq && j == kSChunks - 1 && fst) {
-                            // the rotary query of this range (its buffer was
-                            // reloaded after the previous range's last product)
-                            if (!mbar_wait_fast(&bars->qpe_full, seg & 1, abort_flag, a.status,
-                                                wl)) {
-                                ok = false;
-                                break;
-                            }
-                            ++seg;
-                        }
-                        if (!mbar_wait_fast(&bars->cfull[s], (c / kSSlots) & 1, abort_flag,
-                                            a.status, wl)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t st = smem_u32(ring + s * kSChunk);
-                        if (isq) {
-                            // latent query chunk into TMEM; issued after the
-                            // previous range's products, which the tensor pipe
-                            // runs first
-#pragma unroll
+                            tc_fence_after();
+                            const uint32_t st = smem_u32(from_staging ? msg : ring + s * kSChunk);
                             for (int gg = 0; gg < kSGroups; ++gg) {
                                 const int qg = kSGroups * j + gg;
                                 if (qg >= kQGroups) break;
@@ -413,31 +470,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     tmem_cp_128x256b(tmem + kColQ + 32 * qg + 8 * kk,
                                                      sdesc(st + gg * kGroup + 32 * kk, 16, 1024, 2));
                             }
-                        } else {
-#pragma unroll
-                            for (int gg = 0; gg < kSGroups; ++gg) {
-                                const int cg = kSGroups * j + gg;     // 64-column group 0..8
-                                const uint32_t gt = st + gg * kGroup;
-                                if (cg < kQGroups) {
-#pragma unroll
-                                    for (int kk = 0; kk < 4; ++kk)
-                                        mma_ts(d_s, tmem + kColQ + 32 * cg + 8 * kk,
-                                               sdesc(gt + 32 * kk, 16, 1024, 2), id_s,
-                                               (cg | kk) != 0);
-                                } else {
-                                    // rotary part: Q_pe from shared memory
-#pragma unroll
-                                    for (int kk = 0; kk < 4; ++kk)
-                                        mma_ss(d_s, sdesc(qa + 32 * kk, 16, 1024, 2),
-                                               sdesc(gt + 32 * kk, 16, 1024, 2), id_s, 1);
-                                }
+                            if (!from_staging) {
+                                tc_commit(&bars->cempty[s]);
+                                ++c;
                             }
+                        }
+                        if (!ok) break;
+                        qb = seg & 1;
+                        if (!mbar_wait_fast(&bars->qpe_full[qb], (seg >> 1) & 1, abort_flag,
+                                            a.status, wl))
+                            break;
+                        ++seg;
+                    }
+                    const int sb = k & 1;   // S buffer: the softmax warps read S(k-1) meanwhile
+                    if (!mbar_wait_fast(&bars->s_empty[sb], ((k >> 1) & 1) ^ 1, abort_flag,
+                                        a.status, wl))
+                        break;
+                    tc_fence_after();
+                    const uint32_t d_s = tmem + kColS + 128 * sb;
+                    const uint32_t qa = smem_u32(smem + kQpeOff + qb * kQpeBytes);
+                    for (int j = 0; j < kSChunks; ++j, ++c) {
+                        const int s = c % kSSlots;
+                        if (!mbar_wait_fast(&bars->cfull[s], (c / kSSlots) & 1, abort_flag,
+                                            a.status, wl)) {
+                            ok = false;
+                            break;
+                        }
+                        DECODE_TRACE(j, k);
+                        tc_fence_after();
+                        const uint64_t b0 = sdesc(smem_u32(ring + s * kSChunk), 16, 1024, 2);
+                        if (j == 0) {
+                            // chunk 0: groups 0-2, the tile's first MMA starts the sum
+                            const uint32_t a0 = tmem + kColQ;
+                            mma_ts_new(d_s, a0, b0, id_s);
+#pragma unroll
+                            for (int q = 1; q < 12; ++q)
+                                mma_ts_acc(d_s, a0 + 8 * q, b0 + (uint64_t)(q >> 2) * 1024 + 2 * (q & 3), id_s);
+                        } else if (j == 1) {
+                            const uint32_t a0 = tmem + kColQ + 32 * kSGroups;
+#pragma unroll
+                            for (int q = 0; q < 12; ++q)
+                                mma_ts_acc(d_s, a0 + 8 * q, b0 + (uint64_t)(q >> 2) * 1024 + 2 * (q & 3), id_s);
+                        } else {
+                            // groups 6, 7 (latent) and 8 (rotary part, Q_pe from shared memory)
+                            const uint32_t a0 = tmem + kColQ + 32 * 2 * kSGroups;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                mma_ts_acc(d_s, a0 + 8 * q, b0 + (uint64_t)(q >> 2) * 1024 + 2 * (q & 3), id_s);
+                            const uint64_t qd = sdesc(qa, 16, 1024, 2);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss_acc(d_s, qd + 2 * kk, b0 + 2048 + 2 * kk, id_s);
                         }
                         tc_commit(&bars->cempty[s]);
                     }
                     if (!ok) break;
                     tc_commit(&bars->s_full[sb]);
-                    if (cur.last(hi)) tc_commit(&bars->qpe_free);
+                    DECODE_TRACE(3, k);
+                    if (cur.last(hi)) tc_commit(&bars->qpe_free[qb]);
                 }
             } else {
                 // O += P C, per column half: K = 128 tokens = two 64-token chunks
@@ -446,13 +536,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < K && ok; ++k, cur.next()) {
                     const int slot = k % kMsgSlots;
                     const bool first = cur.first(lo);
-                    mbar_arrive_expect_tx(&bars->p_full[slot], kMsgSent);
+                    mbar_arrive_expect_tx(&bars->p_full[slot], kMsgBytes);
                     if (!mbar_wait_fast<true>(&bars->p_full[slot], (k / kMsgSlots) & 1,
                                               abort_flag, a.status, wl))
                         break;
-                    // P was stored by the peer's threads: make it visible to
-                    // the tensor core's reads
-                    fence_proxy_async();
+                    DECODE_TRACE(0, k);
                     const uint8_t* m = msg + slot * kMsgBytes;
                     const int* aux = (const int*)(m + kPBytes);
                     const bool need_resc =
@@ -469,7 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         !mbar_wait_fast(&bars->zeroed, (zer++) & 1, abort_flag, a.status, wl))
                         break;
                     tc_fence_after();
-                    const uint32_t pa = smem_u32(m);
+                    const uint64_t pdesc = sdesc(smem_u32(m), 16, 1024, 2);
                     for (int j = 0; j < kVChunks; ++j, ++c) {
                         const int s = c % kVSlots, hh = j >> 1, pg = j & 1;
                         if (!mbar_wait_fast(&bars->cfull[s], (c / kVSlots) & 1, abort_flag,
@@ -477,18 +565,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
+                        if (j == 0) DECODE_TRACE(1, k);
+                        if (j == kVChunks - 1) DECODE_TRACE(2, k);
                         tc_fence_after();
-                        const uint32_t st = smem_u32(ring + s * kVChunk);
+                        const uint64_t bd = sdesc(smem_u32(ring + s * kVChunk), kBox, 1024, 2);
+                        const uint64_t ad = pdesc + (uint64_t)pg * (kPBytes / 2 / 16);
+                        const uint32_t dst = tmem + kColO + 256 * hh;
+                        if (pg == 0)
+                            mma_ss(dst, ad, bd, id_pv, first ? 0 : 1);
+                        else
+                            mma_ss_acc(dst, ad, bd, id_pv);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            mma_ss(tmem + kColO + 256 * hh,
-                                   sdesc(pa + pg * (kPBytes / 2) + 32 * i, 16, 1024, 2),
-                                   sdesc(st + 2048 * i, kBox, 1024, 2), id_pv,
-                                   (first && pg == 0 && i == 0) ? 0 : 1);
+                        for (int i = 1; i < 4; ++i) mma_ss_acc(dst, ad + 2 * i, bd + 128 * i, id_pv);
                         tc_commit(&bars->cempty[s]);
                     }
                     if (!ok) break;
                     tc_commit(&bars->pv_done[slot]);
+                    DECODE_TRACE(3, k);
                     if (cur.last(hi)) ++seg;
                 }
             }
@@ -512,9 +605,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float c2 = a.scale * 1.4426950408889634f;   // log2(e) / sqrt(d)
             const uint32_t msg_peer = mapa(smem_u32(msg), 1);
             const uint32_t pfull_peer = mapa(smem_u32(&bars->p_full[0]), 1);
-            // exchange between the two threads of a head: tile maxima (two
-            // buffers by tile parity) and the row sums of a range's last tile
-            float* red = (float*)(smem + kRedOff);
+            float* red = (float*)(smem + kRedOff);     // [2][128] per-half tile max
 
             // rendezvous of the 256 softmax threads: an mbarrier with a bounded
             // wait, so a timeout anywhere releases everyone
@@ -525,7 +616,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             };
 
             float m = -INFINITY, l = 0.f;     // m: running max (log2 units); l: this half's sum
-            int sent = 0;                     // messages stored into the value CTA
             for (int k = 0; k < K; ++k, cur.next()) {
                 const int b = cur.b;
                 const bool first = cur.first(lo), last = cur.last(hi);
@@ -533,44 +623,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int nv = tr.valid[half];          // valid tokens of this thread's 64
                 const int buf = k % kMsgSlots;
 
-                // ---- this thread's 64 scores
+                // ---- this thread's 64 scores, read from TMEM in four 16-column
+                // pieces: a first pass takes the maximum, a second one the
+                // weights (runtime loops keep this hot code small)
                 const int sb = k & 1;
                 if (!mbar_wait_fast(&bars->s_full[sb], (k >> 1) & 1, abort_flag, a.status, wl))
                     break;
+                if (tid == 0) DECODE_TRACE(4, k);
                 tc_fence_after();
-                float sv[kHalf];
-                {
-                    const uint32_t src = tmem + lane_off + kColS + 128 * sb + 64 * half;
-                    uint32_t r[64];
-                    MLA_TMEM_LD_X32(src, r);
-                    MLA_TMEM_LD_X32(src + 32, (r + 32));
+                const uint32_t src = tmem + lane_off + kColS + 128 * sb + 64 * half;
+                float mloc = -INFINITY;
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t r[16];
+                    MLA_TMEM_LD_X16(src + 16 * c4, r);
                     tmem_ld_wait();
+                    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < kHalf; ++i) sv[i] = __uint_as_float(r[i]);
-                }
-                tc_fence_before();
-                mbar_arrive(&bars->s_empty[sb]);
-
-                // ---- tile max of the raw scores (the scale is positive)
-                float mx[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) mx[j] = -INFINITY;
-                if (nv == kHalf) {
-#pragma unroll
-                    for (int i = 0; i < kHalf; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < kHalf; ++i) {
-                        if (i >= nv) sv[i] = -INFINITY;
-                        mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
+                    for (int i = 0; i < 16; i += 2) {
+                        const float v0 = 16 * c4 + i < nv ? __uint_as_float(r[i]) : -INFINITY;
+                        const float v1 = 16 * c4 + i + 1 < nv ? __uint_as_float(r[i + 1]) : -INFINITY;
+                        mx0 = fmaxf(mx0, v0);
+                        mx1 = fmaxf(mx1, v1);
                     }
+                    mloc = fmaxf(mloc, fmaxf(mx0, mx1));
                 }
-                float mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                float* tmax = red + (k & 1) * 2 * kHeads;
-                tmax[half * kHeads + h] = mloc;
+                // the staging buffer is free once the copy of tile k-1 read it
+                if (tid == 0) bulk_wait_read<0>();
+                red[half * kHeads + h] = mloc;
                 if (!wg_sync()) break;
-                const float mt = fmaxf(mloc, tmax[(half ^ 1) * kHeads + h]) * c2;
+                const float mt = fmaxf(mloc, red[(half ^ 1) * kHeads + h]) * c2;
 
                 // ---- online softmax (log2 domain), lazy rescale; both threads
                 // of a head take the same decisions from the same values
@@ -583,57 +665,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 const bool resc = grow && !first;
 
-                // ---- the value CTA's receive slot for this tile must be free
-                // (its products and reads of message k-2 are done)
-                if (!mbar_wait_fast<true>(&bars->p_empty[buf], ((k / kMsgSlots) & 1) ^ 1,
-                                          abort_flag, a.status, wl))
-                    break;
-                const uint32_t dst = msg_peer + buf * kMsgBytes;
-                const uint32_t bar = pfull_peer + 8 * buf;
-
-                // ---- P: bf16 weights, 8 tokens = one 16-byte chunk at a time,
-                // in the 128-byte-swizzled K-major layout of the PV operand,
-                // stored straight into the value CTA's receive slot
-                const uint32_t row = dst + half * (kPBytes / 2) + h * 128;
+                // ---- P: bf16 weights, two 16-byte chunks (16 tokens) per piece,
+                // in the 128-byte-swizzled K-major layout of the PV operand
+                uint8_t* mb = msg;     // the one staging buffer
+                uint8_t* row = mb + half * (kPBytes / 2) + h * 128;
                 const float nm = m == -INFINITY ? 0.f : -m;   // all-masked tile: p = 0
-                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t r[16];
+                    MLA_TMEM_LD_X16(src + 16 * c4, r);
+                    tmem_ld_wait();
+                    uint32_t w[8];
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float v0 = sv[8 * cc + 2 * i], v1 = sv[8 * cc + 2 * i + 1];
-                        // masked scores are -inf and give exp2(-inf) = 0
-                        const float p0 = ex2(fmaf(v0, c2, nm));
-                        const float p1 = ex2(fmaf(v1, c2, nm));
-                        ps[i] += p0 + p1;
+                    for (int i = 0; i < 8; ++i) {
+                        const int t = 16 * c4 + 2 * i;
+                        // tokens past the valid ones weigh 0
+                        const float p0 = t < nv ? ex2(fmaf(__uint_as_float(r[2 * i]), c2, nm)) : 0.f;
+                        const float p1 = t + 1 < nv ? ex2(fmaf(__uint_as_float(r[2 * i + 1]), c2, nm)) : 0.f;
+                        ps0 += p0;
+                        ps1 += p1;
                         w[i] = pack_bf16(p0, p1);
                     }
-                    st_async_u4(row + ((cc ^ (h & 7)) * 16), w[0], w[1], w[2], w[3], bar);
+                    const int cc = 2 * c4;
+                    *(uint4*)(row + ((cc ^ (h & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *(uint4*)(row + (((cc + 1) ^ (h & 7)) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
-                l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                tc_fence_before();
+                mbar_arrive(&bars->s_empty[sb]);
+                l += ps0 + ps1;
 
-                // ---- aux block: factors (one per head), this half's row sums,
-                // per-warp rescale flags, valid rows of the two halves
-                const uint32_t aux = dst + kPBytes;
+                float* aux = (float*)(mb + kPBytes);
                 if (half == 0) {
-                    st_async_b32(aux + 4 * (kAuxAlpha + h), __float_as_uint(resc ? alpha : 1.f),
-                                 bar);
+                    aux[kAuxAlpha + h] = resc ? alpha : 1.f;
                     const bool any = __any_sync(0xffffffffu, resc);
-                    if (lane == 0) st_async_b32(aux + 4 * (kAuxFlags + q4), any ? 1u : 0u, bar);
+                    if (lane == 0) ((int*)aux)[kAuxFlags + q4] = any ? 1 : 0;
                 }
-                st_async_b32(aux + 4 * (kAuxSum + half * kHeads + h), __float_as_uint(l), bar);
+                if (last) aux[kAuxSum + half * kHeads + h] = l;
                 if (tid == 0) {
-                    st_async_b32(aux + 4 * kAuxValid, (uint32_t)tr.valid[0], bar);
-                    st_async_b32(aux + 4 * (kAuxValid + 1), (uint32_t)tr.valid[1], bar);
+                    ((int*)aux)[kAuxValid] = tr.valid[0];
+                    ((int*)aux)[kAuxValid + 1] = tr.valid[1];
                 }
-                ++sent;
+                fence_proxy_async();
+                if (last) red[kHeads * 2 + half * kHeads + h] = l;
+                if (!wg_sync()) break;
+                if (tid == 0 && mbar_wait_fast<true>(&bars->p_empty[buf],
+                                                     ((k / kMsgSlots) & 1) ^ 1, abort_flag,
+                                                     a.status, wl)) {
+                    DECODE_TRACE(5, k);
+                    bulk_s2s(msg_peer + buf * kMsgBytes, smem_u32(mb), kMsgBytes,
+                             pfull_peer + 8 * buf);
+                    bulk_commit();
+                    DECODE_TRACE(6, k);
+                }
                 if (last) {
-                    float* sums = red + 4 * kHeads;
-                    sums[half * kHeads + h] = l;
-                    if (!wg_sync()) break;
                     if (half == 0) {
-                        const float lt = l + sums[kHeads + h];
+                        const float lt = l + red[kHeads * 3 + h];
                         a.lse_part[((size_t)g + b) * kHeads + h] =
                             lt > 0.f ? (m + __log2f(lt)) * 0.6931471805599453f : -INFINITY;
                     }
@@ -641,12 +728,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     l = 0.f;
                 }
             }
-            // The stores into the value CTA land before this CTA leaves: wait
-            // (bounded) until the value CTA has released the last messages'
-            // slots, which it does only after they arrived and were used.
-            if (tid == 0)
-                for (int i = sent > kMsgSlots ? sent - kMsgSlots : 0; i < sent; ++i)
-                    drain_wait(&bars->p_empty[i % kMsgSlots], (i / kMsgSlots) & 1);
+            if (tid == 0) bulk_wait_all();
         } else {
             // ------------------------------------------ value-CTA warpgroup:
             // rare O rescales, zeroing of rows past a sequence end, the
@@ -683,6 +765,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     if (__any_sync(0xffffffffu, alpha != 1.f)) {
                         uint32_t r[32];
+#pragma unroll 1
                         for (int cc = 0; cc < 256; cc += 32) {
                             MLA_TMEM_LD_X32(tmem + lane_off + col0 + cc, r);
                             tmem_ld_wait();
@@ -723,16 +806,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!mbar_wait_fast(&bars->pv_done[slot], (k / kMsgSlots) & 1, abort_flag,
                                     a.status, wl))
                     break;
+                if (tid == 0) DECODE_TRACE(4, k);
                 if (last) {
                     // ---- the range's normalised partial.  A warp holds a
                     // 32-head x 32-column block per TMEM load (one row per
-                    // thread); it goes through 4 KB of the consumed receive slot
+                    // thread); it goes through 4 KB of the consumed message slot
                     // so that each store instruction writes whole 128-byte rows.
                     tc_fence_after();
                     float* xb = (float*)(msg + slot * kMsgBytes) + (warp - 2) * 1024;
                     float* dst0 = a.o_part + (((size_t)g + b) * kHeads + q4 * 32) * kDL +
                                   256 * half;
                     uint32_t r[32];
+#pragma unroll 1
                     for (int cc = 0; cc < 256; cc += 32) {
                         MLA_TMEM_LD_X32(tmem + lane_off + col0 + cc, r);
                         tmem_ld_wait();
@@ -752,11 +837,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp();
                     }
-                    fence_proxy_async();   // the next stores into this slot come after
+                    fence_proxy_async();   // the next bulk copy into this slot comes after
                     tc_fence_before();
+                    if (tid == 0) DECODE_TRACE(5, k);
                     mbar_arrive(&bars->o_free);
                 }
-                // the receive slot (P and its aux block) may be overwritten now
+                // the message slot (P and its factors) may be overwritten now
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(pempty_peer + 8 * slot);
             }
@@ -811,6 +897,16 @@ bool decode_tc_supported(int heads, int d_latent, int d_rope, int block_size, in
 
 int decode_tc_tile() { return kT; }
 
+#ifdef MLA_DECODE_TRACE
+extern "C" int mla_decode_trace_copy(unsigned long long* tiles, unsigned long long* ctas) {
+    cudaDeviceSynchronize();
+    if (cudaMemcpyFromSymbol(tiles, g_decode_trace, sizeof(g_decode_trace)) != cudaSuccess ||
+        cudaMemcpyFromSymbol(ctas, g_decode_trace_cta, sizeof(g_decode_trace_cta)) != cudaSuccess)
+        return 1;
+    return 0;
+}
+#endif
+
 // Clusters that can be resident at once (pairs of SMs within one GPC), at most
 // one per SM pair.  Computed once per device.
 int decode_tc_workers(int num_sms) {
@@ -837,7 +933,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
         return cudaErrorInvalidValue;
     DeviceState* d = device_state();
     if (!d || !d->attr) return cudaErrorNotSupported;
-    CUtensorMap t_cache, t_chunk, t_page, t_qlat, t_qpe;
+    CUtensorMap t_cache, t_chunk, t_page, t_qlat, t_qpe, t_qlat2;
     const uint64_t rows = (uint64_t)a.num_blocks * a.block_size;
     // cache rows, 64 x 64 boxes
     const uint64_t dims[2] = {(uint64_t)kD, rows};
@@ -855,13 +951,15 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
     const uint64_t dq[3] = {64, qrows, (uint64_t)kQGroups};
     const uint64_t sq[2] = {(uint64_t)kDL * 2, 128};
     const uint32_t bq3[3] = {64, kHeads, kSGroups};
+    const uint32_t bq2[3] = {64, kHeads, kQGroups - 2 * kSGroups};   // last two groups
     const uint64_t dp[2] = {(uint64_t)kDR, qrows}, sp[1] = {(uint64_t)kDR * 2};
     const uint32_t bq[2] = {64, kHeads};
     if (!make_tmap_bf16(&t_cache, a.cache, 2, dims, strides, box, 128) ||
         !make_tmap_bf16(&t_chunk, a.cache, 3, dims3, strides3, boxc, 128) ||
         !make_tmap_bf16(&t_page, a.cache, 3, dims3, strides3, box3, 128) ||
         !make_tmap_bf16(&t_qlat, a.q_lat, 3, dq, sq, bq3, 128) ||
-        !make_tmap_bf16(&t_qpe, a.q_pe, 2, dp, sp, bq, 128))
+        !make_tmap_bf16(&t_qpe, a.q_pe, 2, dp, sp, bq, 128) ||
+        !make_tmap_bf16(&t_qlat2, a.q_lat, 3, dq, sq, bq2, 128))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * a.workers);
@@ -874,7 +972,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_tc_kernel, t_cache, t_chunk, t_page, t_qlat, t_qpe,
-                              a);
+                              t_qlat2, a);
 }
 
 }  // namespace mla

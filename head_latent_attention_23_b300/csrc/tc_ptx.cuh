@@ -105,13 +105,12 @@ __device__ __forceinline__ bool mbar_poll_cluster(uint32_t addr, uint32_t parity
 // Bounded wait without suspend hints, for the per-tile handshakes of the
 // decode pipeline.  Same give-up rule as mbar_wait, after `limit_ns`
 // (kWaitLimitNs unless a caller lowers it; a limit under 100 us is checked
-// after every poll so that it trips reliably).
-template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity,
-                                               volatile int* abort, int* status,
-                                               uint64_t limit_ns = kWaitLimitNs) {
-    const uint32_t a = smem_u32(bar);
-    if (kCluster ? mbar_poll_cluster(a, parity) : mbar_poll(a, parity)) return true;
+// after every poll so that it trips reliably).  The first poll is inline;
+// the polling loop is a separate, not inlined function, so that a kernel
+// with dozens of waits keeps its hot loops small.
+template <bool kCluster>
+__device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, volatile int* abort,
+                                            int* status, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     const uint32_t every = limit_ns < 100000ull ? 0u : 63u;
     for (uint32_t i = 1;; ++i) {
@@ -125,6 +124,14 @@ __device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity,
             }
         }
     }
+}
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, int* status,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+    const uint32_t a = smem_u32(bar);
+    if (kCluster ? mbar_poll_cluster(a, parity) : mbar_poll(a, parity)) return true;
+    return mbar_wait_slow<kCluster>(a, parity, abort, status, limit_ns);
 }
 
 // Bounded wait for the phase of `bar` with parity `parity` to complete.
