@@ -15,9 +15,10 @@ ours:       device-resident inputs; R replicas of every input tensor are
             weights in L2 (R * bytes > 2 * L2).  The steps' library calls are
             captured once into CUDA graphs and replayed; CUDA events on the
             launching stream time the replays (and, inside the graph, each
-            mla_decode call); max over ranks.  e2e: the same step preceded by pinned
-            host -> device copies of the step's inputs and followed by a
-            device -> host read of its output.
+            mla_decode call); max over ranks.  e2e: the same step through one
+            library call per step (mla_cached_decode_step or
+            mla_layer_decode_step) with pinned HOST inputs and output, the
+            copies inside the call and inside the timed region.
 reference:  the fp64 CPU oracle (unmerged MLA) on a bounded sample of the
             same workload, on the host cores.
 """
@@ -375,7 +376,8 @@ def run_ours(args):
     # end to end: pinned host inputs -> device, step, result -> host
     if ws > 1:
         dist.barrier()
-    e2e = run_e2e(steps[0], w, dev, stream, max(20, min(K, 2000)))
+    e2e = run_e2e(steps[0], w, dev, stream) if steps[0].fused else \
+        {"value": None, "unit": UNIT, "note": "workload appends several rows per sequence"}
 
     if rank != 0:
         if ws > 1:
@@ -476,41 +478,53 @@ def _run_with_decode_events(s, evpair, stream):
         mla.project_out(s.cfg, s.o_lat, s.w_uv, s.o_v)
 
 
-def run_e2e(s, w, dev, stream, K):
-    """Same step through the public calls, with the step's inputs copied from
-    pinned host memory and its output read back every step."""
+def run_e2e(s, w, dev, stream, min_steps=500, min_seconds=1.0):
+    """The step end to end through one public library call per step
+    (mla_cached_decode_step or mla_layer_decode_step) with HOST buffers: the
+    call copies the step's inputs from pinned host memory, runs the kernels
+    and copies the result back, all inside the timed region.  At least
+    `min_steps` steps and about `min_seconds`, whatever --steps says."""
     if s.kind == "cached":
-        ins = [("q_nope", s.q_nope), ("q_pe", s.q_pe), ("seq_lens", s.seq_lens),
-               ("block_table", s.block_table)]
+        names = ["q_nope", "q_pe", "seq_lens", "block_table"]
         result = s.o_v
     else:
-        ins = [("x_q", s.x_q), ("pos_q", s.pos_q), ("x_new", s.x_new),
-               ("seq_lens", s.seq_lens), ("block_table", s.block_table)]
+        names = ["x", "seq_lens", "block_table"]
         result = s.out
-    host_in = [(d, d.cpu().pin_memory()) for _, d in ins]
+    dev_t = dict(q_nope=s.q_nope, q_pe=s.q_pe, seq_lens=s.seq_lens, block_table=s.block_table)
+    if s.kind != "cached":
+        dev_t["x"] = s.x_q
+    host_in = {n: dev_t[n].cpu().pin_memory() for n in names}
     host_out = torch.empty(result.shape, dtype=result.dtype).pin_memory()
-    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
+    h2d = sum(h.numel() * h.element_size() for h in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
-    for _ in range(3):
-        for d, h in host_in:
-            d.copy_(h, non_blocking=True)
-        s.run()
-        host_out.copy_(result, non_blocking=True)
+    flags = 3   # MLA_IO_HOST_INPUTS | MLA_IO_HOST_OUTPUT
+
+    def step():
+        s.run_fused(io_flags=flags, inputs=host_in, result=host_out)
+
+    for _ in range(5):
+        step()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    for _ in range(50):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    per = a.elapsed_time(b) / 50 / 1e3
+    K = int(max(min_steps, min(min_seconds / max(per, 1e-7), 200000)))
+    a.record(stream)
     for _ in range(K):
-        for d, h in host_in:
-            d.copy_(h, non_blocking=True)
-        s.run()
-        host_out.copy_(result, non_blocking=True)
+        step()
     b.record(stream)
     torch.cuda.synchronize()
     value, total = job_rate(a.elapsed_time(b), w["batch"] * K, dev)
     ms = total / K
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K,
-            "note": "same input set every step (L2-warm weights and cache)"}
+            "call": "mla_cached_decode_step" if s.kind == "cached" else "mla_layer_decode_step",
+            "note": ("one library call per step with pinned host inputs and output; "
+                     "same input set every step")}
 
 
 def main():

@@ -125,4 +125,23 @@ cudaError_t launch_q_split_rope(const float* q_all, int batch, int heads, int d_
     return cudaGetLastError();
 }
 
+// Position and sequence index of each sequence's newest token for one
+// decode step: pos[b] = seq_lens[b] - 1 (the query and the appended row sit
+// at the last position), seq_idx[b] = b.  A length below 1 gives pos -1,
+// which the append flags as an invalid slot.
+__global__ void step_positions_kernel(const int32_t* __restrict__ seq_lens, int batch,
+                                      int32_t* __restrict__ pos, int32_t* __restrict__ seq_idx) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= batch) return;
+    const int n = seq_lens[b];
+    pos[b] = n >= 1 ? n - 1 : -1;
+    seq_idx[b] = b;
+}
+
+cudaError_t launch_step_positions(const int32_t* seq_lens, int batch, int32_t* pos,
+                                  int32_t* seq_idx, cudaStream_t st) {
+    step_positions_kernel<<<(batch + 255) / 256, 256, 0, st>>>(seq_lens, batch, pos, seq_idx);
+    return cudaGetLastError();
+}
+
 }  // namespace mla

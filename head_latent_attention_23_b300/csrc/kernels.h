@@ -84,6 +84,10 @@ cudaError_t launch_q_split_rope(const float* q_all, int batch, int heads, int d_
                                 int d_rope, const int32_t* pos, double rope_base, void* q_nope,
                                 void* q_pe, int dtype, cudaStream_t st);
 
+// pos[b] = seq_lens[b] - 1, seq_idx[b] = b (device arrays of one decode step).
+cudaError_t launch_step_positions(const int32_t* seq_lens, int batch, int32_t* pos,
+                                  int32_t* seq_idx, cudaStream_t st);
+
 // ---------------------------------------------------------------- tcgen05 GEMM
 // A bf16 operand seen by TMA as a 3-D array: dims[0] innermost (elements),
 // strides[i] = byte stride of dims[i+1].  A: {K, M, batch}.  B: {K, N, batch}

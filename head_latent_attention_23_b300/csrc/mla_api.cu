@@ -406,6 +406,214 @@ int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, co
                                        cfg->rope_base, q_nope, q_pe, cfg->dtype, st));
 }
 
+// ---------------------------------------------------------------------------
+// Whole decode steps in one call.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+size_t dtype_size(const mla_config* c) { return c->dtype == MLA_DTYPE_BF16 ? 2 : 4; }
+
+// Sequential carving of a workspace into 256-byte aligned pieces.  With a
+// null base it only counts bytes.
+struct Carver {
+    char* base;
+    size_t used;
+    void* take(size_t bytes) {
+        void* p = base ? base + used : nullptr;
+        used += align256(bytes);
+        return p;
+    }
+};
+
+// Per-step inputs that the caller may pass in host memory: copied into the
+// workspace on the stream (cudaMemcpyAsync, one per tensor).
+int stage_in(const void** ptr, void* dev, size_t bytes, bool host, cudaStream_t st) {
+    if (!host) return MLA_OK;
+    if (cudaMemcpyAsync(dev, *ptr, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    *ptr = dev;
+    return MLA_OK;
+}
+
+struct LayerWs {
+    int32_t *seq_lens, *block_table, *pos, *seq_idx;
+    void *x, *q_nope, *q_pe, *q_lat, *o_lat, *o_v, *out, *q_scratch, *dec;
+    size_t q_scratch_bytes, dec_bytes;
+};
+
+int layer_ws(const mla_config* c, const mla_layer_weights* w, int batch, int max_blocks,
+             char* base, LayerWs* ws, size_t* total) {
+    const size_t es = dtype_size(c), B = (size_t)batch, H = (size_t)c->heads;
+    int W;
+    if (int rc = decode_workers(c, batch, &W)) return rc;
+    size_t qs;
+    if (int rc = mla_query_proj_workspace_size(c, batch, w->w_dq ? w->d_lq : 0, &qs)) return rc;
+    Carver k{base, 0};
+    ws->seq_lens = (int32_t*)k.take(B * 4);
+    ws->block_table = (int32_t*)k.take(B * (size_t)max_blocks * 4);
+    ws->pos = (int32_t*)k.take(B * 4);
+    ws->seq_idx = (int32_t*)k.take(B * 4);
+    ws->x = k.take(B * (size_t)w->d_model * es);
+    ws->q_nope = k.take(B * H * c->d_nope * es);
+    ws->q_pe = k.take(B * H * c->d_rope * es);
+    ws->q_lat = k.take(B * H * c->d_latent * es);
+    ws->o_lat = k.take(B * H * c->d_latent * es);
+    ws->o_v = k.take(B * H * c->d_v * es);
+    ws->out = k.take(B * (size_t)w->d_model * es);
+    ws->q_scratch_bytes = qs;
+    ws->q_scratch = k.take(qs);
+    ws->dec_bytes = decode_ws_bytes(c, W, batch);
+    ws->dec = k.take(ws->dec_bytes);
+    *total = k.used;
+    return MLA_OK;
+}
+
+struct CachedWs {
+    int32_t *seq_lens, *block_table;
+    void *q_nope, *q_pe, *q_lat, *o_lat, *o_v, *dec;
+    float* lse;
+    size_t dec_bytes;
+};
+
+int cached_ws(const mla_config* c, int batch, int max_blocks, char* base, CachedWs* ws,
+              size_t* total) {
+    const size_t es = dtype_size(c), B = (size_t)batch, H = (size_t)c->heads;
+    int W;
+    if (int rc = decode_workers(c, batch, &W)) return rc;
+    Carver k{base, 0};
+    ws->seq_lens = (int32_t*)k.take(B * 4);
+    ws->block_table = (int32_t*)k.take(B * (size_t)max_blocks * 4);
+    ws->q_nope = k.take(B * H * c->d_nope * es);
+    ws->q_pe = k.take(B * H * c->d_rope * es);
+    ws->q_lat = k.take(B * H * c->d_latent * es);
+    ws->o_lat = k.take(B * H * c->d_latent * es);
+    ws->lse = (float*)k.take(B * H * 4);
+    ws->o_v = k.take(B * H * c->d_v * es);
+    ws->dec_bytes = decode_ws_bytes(c, W, batch);
+    ws->dec = k.take(ws->dec_bytes);
+    *total = k.used;
+    return MLA_OK;
+}
+
+bool valid_weights(const mla_layer_weights* w) {
+    return w && w->d_model >= 1 && w->w_dkv && w->w_uq && w->w_uk && w->w_uv && w->w_o &&
+           (!w->w_dq || w->d_lq >= 1);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_layer_decode_step_workspace_size(const mla_config* cfg, const mla_layer_weights* w,
+                                         int batch, int max_blocks, size_t* bytes) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (!bytes || !valid_weights(w) || batch < 1 || batch > kMaxDecodeBatch || max_blocks < 1)
+        return MLA_ERR_INVALID_ARG;
+    LayerWs ws;
+    return layer_ws(cfg, w, batch, max_blocks, nullptr, &ws, bytes);
+}
+
+int mla_layer_decode_step(const mla_config* cfg, const mla_layer_weights* w, const void* x,
+                          const int32_t* seq_lens, int batch, void* cache, int64_t num_blocks,
+                          const int32_t* block_table, int max_blocks, void* out, int io_flags,
+                          void* workspace, size_t ws_bytes, mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (!valid_weights(w) || batch < 1 || batch > kMaxDecodeBatch || max_blocks < 1 ||
+        num_blocks < 1 || (io_flags & ~(MLA_IO_HOST_INPUTS | MLA_IO_HOST_OUTPUT)))
+        return MLA_ERR_INVALID_ARG;
+    if (!x || !seq_lens || !cache || !block_table || !out) return MLA_ERR_INVALID_ARG;
+    LayerWs ws;
+    size_t need;
+    if (int rc = layer_ws(cfg, w, batch, max_blocks, (char*)workspace, &ws, &need)) return rc;
+    if (!workspace || ws_bytes < need || ((uintptr_t)workspace & 255)) return MLA_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool hin = io_flags & MLA_IO_HOST_INPUTS, hout = io_flags & MLA_IO_HOST_OUTPUT;
+    const size_t es = dtype_size(cfg);
+    const void* xs = x;
+    const void* sl = seq_lens;
+    const void* bt = block_table;
+    if (int rc = stage_in(&xs, ws.x, (size_t)batch * w->d_model * es, hin, st)) return rc;
+    if (int rc = stage_in(&sl, ws.seq_lens, (size_t)batch * 4, hin, st)) return rc;
+    if (int rc = stage_in(&bt, ws.block_table, (size_t)batch * max_blocks * 4, hin, st)) return rc;
+    if (launch_step_positions((const int32_t*)sl, batch, ws.pos, ws.seq_idx, st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    mla_stream_t s = stream;
+    if (int rc = mla_query_proj(cfg, xs, batch, w->d_model, w->w_dq, w->w_dq ? w->d_lq : 0,
+                                w->w_uq, ws.pos, ws.q_nope, ws.q_pe, ws.q_scratch,
+                                ws.q_scratch_bytes, s))
+        return rc;
+    if (int rc = mla_append_latent(cfg, xs, batch, w->d_model, w->w_dkv, ws.seq_idx, ws.pos,
+                                   (const int32_t*)bt, batch, max_blocks, cache, num_blocks,
+                                   nullptr, s))
+        return rc;
+    if (int rc = mla_absorb_q(cfg, ws.q_nope, w->w_uk, batch, ws.q_lat, s)) return rc;
+    if (int rc = mla_decode(cfg, ws.q_lat, ws.q_pe, cache, num_blocks, (const int32_t*)bt,
+                            max_blocks, (const int32_t*)sl, batch, ws.o_lat, nullptr, ws.dec,
+                            ws.dec_bytes, s))
+        return rc;
+    void* o = hout ? ws.out : out;
+    if (int rc = mla_project_out(cfg, ws.o_lat, w->w_uv, batch, ws.o_v, w->w_o, w->d_model, o, s))
+        return rc;
+    if (hout && cudaMemcpyAsync(out, ws.out, (size_t)batch * w->d_model * es,
+                                cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    return MLA_OK;
+}
+
+int mla_cached_decode_step_workspace_size(const mla_config* cfg, int batch, int max_blocks,
+                                          size_t* bytes) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (!bytes || batch < 1 || batch > kMaxDecodeBatch || max_blocks < 1)
+        return MLA_ERR_INVALID_ARG;
+    CachedWs ws;
+    return cached_ws(cfg, batch, max_blocks, nullptr, &ws, bytes);
+}
+
+int mla_cached_decode_step(const mla_config* cfg, const void* q_nope, const void* q_pe,
+                           const void* w_uk, const void* w_uv, const int32_t* seq_lens,
+                           int batch, const void* cache, int64_t num_blocks,
+                           const int32_t* block_table, int max_blocks, void* o_v, void* o_lat,
+                           float* lse, int io_flags, void* workspace, size_t ws_bytes,
+                           mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (batch < 1 || batch > kMaxDecodeBatch || max_blocks < 1 || num_blocks < 1 ||
+        (io_flags & ~(MLA_IO_HOST_INPUTS | MLA_IO_HOST_OUTPUT)))
+        return MLA_ERR_INVALID_ARG;
+    if (!q_nope || (!q_pe && cfg->d_rope > 0) || !w_uk || !w_uv || !seq_lens || !cache ||
+        !block_table || !o_v)
+        return MLA_ERR_INVALID_ARG;
+    CachedWs ws;
+    size_t need;
+    if (int rc = cached_ws(cfg, batch, max_blocks, (char*)workspace, &ws, &need)) return rc;
+    if (!workspace || ws_bytes < need || ((uintptr_t)workspace & 255)) return MLA_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool hin = io_flags & MLA_IO_HOST_INPUTS, hout = io_flags & MLA_IO_HOST_OUTPUT;
+    const size_t es = dtype_size(cfg), BH = (size_t)batch * cfg->heads;
+    const void* qn = q_nope;
+    const void* qp = q_pe;
+    const void* sl = seq_lens;
+    const void* bt = block_table;
+    if (int rc = stage_in(&qn, ws.q_nope, BH * cfg->d_nope * es, hin, st)) return rc;
+    if (cfg->d_rope > 0)
+        if (int rc = stage_in(&qp, ws.q_pe, BH * cfg->d_rope * es, hin, st)) return rc;
+    if (int rc = stage_in(&sl, ws.seq_lens, (size_t)batch * 4, hin, st)) return rc;
+    if (int rc = stage_in(&bt, ws.block_table, (size_t)batch * max_blocks * 4, hin, st)) return rc;
+    void* ol = o_lat ? o_lat : ws.o_lat;
+    float* ls = lse ? lse : ws.lse;
+    void* ov = hout ? ws.o_v : o_v;
+    if (int rc = mla_absorb_q(cfg, qn, w_uk, batch, ws.q_lat, stream)) return rc;
+    if (int rc = mla_decode(cfg, ws.q_lat, qp, cache, num_blocks, (const int32_t*)bt, max_blocks,
+                            (const int32_t*)sl, batch, ol, ls, ws.dec, ws.dec_bytes, stream))
+        return rc;
+    if (int rc = mla_project_out(cfg, ol, w_uv, batch, ov, nullptr, 0, nullptr, stream)) return rc;
+    if (hout && cudaMemcpyAsync(o_v, ws.o_v, BH * cfg->d_v * es, cudaMemcpyDeviceToHost, st) !=
+                    cudaSuccess)
+        return MLA_ERR_CUDA;
+    return MLA_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -31,14 +31,25 @@ EXPORTS = (
     "mla_status_string", "mla_version", "mla_decode_path", "mla_get_status",
     "mla_append_latent", "mla_absorb_q", "mla_decode_workspace_size", "mla_decode",
     "mla_decode_combine", "mla_project_out", "mla_query_proj_workspace_size", "mla_query_proj",
-    "mla_decode_noalloc", "mla_set_wait_limit_ns",
+    "mla_decode_noalloc", "mla_set_wait_limit_ns", "mla_layer_decode_step_workspace_size",
+    "mla_layer_decode_step", "mla_cached_decode_step_workspace_size", "mla_cached_decode_step",
 )
+
+IO_HOST_INPUTS = 1
+IO_HOST_OUTPUT = 2
 
 
 class MLAError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
         super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class LayerWeights(ctypes.Structure):
+    """mirror of struct mla_layer_weights (device pointers)"""
+    _fields_ = [("d_model", ctypes.c_int), ("d_lq", ctypes.c_int), ("w_dkv", ctypes.c_void_p),
+                ("w_dq", ctypes.c_void_p), ("w_uq", ctypes.c_void_p), ("w_uk", ctypes.c_void_p),
+                ("w_uv", ctypes.c_void_p), ("w_o", ctypes.c_void_p)]
 
 
 class Config(ctypes.Structure):
@@ -96,6 +107,13 @@ def lib():
         L.mla_query_proj.argtypes = [CP, P, I, I, P, I, P, P, P, P, P, ctypes.c_size_t, P]
         L.mla_decode_noalloc.argtypes = [CP, P, P, P, I64, P, I, P, I, P, P, P]
         L.mla_set_wait_limit_ns.argtypes = [I64]
+        LW = ctypes.POINTER(LayerWeights)
+        L.mla_layer_decode_step_workspace_size.argtypes = [CP, LW, I, I, SZ]
+        L.mla_layer_decode_step.argtypes = [CP, LW, P, P, I, P, I64, P, I, P, I, P,
+                                            ctypes.c_size_t, P]
+        L.mla_cached_decode_step_workspace_size.argtypes = [CP, I, I, SZ]
+        L.mla_cached_decode_step.argtypes = [CP, P, P, P, P, P, I, P, I64, P, I, P, P, P, I, P,
+                                             ctypes.c_size_t, P]
         for name in EXPORTS:
             if name not in ("mla_status_string", "mla_version"):
                 getattr(L, name).restype = I
@@ -255,3 +273,80 @@ def query_proj(cfg, x, w_uq, pos, q_nope, q_pe, w_dq=None, scratch=None, stream=
         _ptr(q_pe, dt, "q_pe"), _ptr(scratch, None, "scratch"),
         scratch.numel() * scratch.element_size(), _stream(stream))
     _check(rc, "mla_query_proj")
+
+
+# ---------------------------------------------------------------- whole steps
+
+def _ptr_io(t, dtype, name, host):
+    """Device pointer, or (host=True) pointer of a pinned, contiguous CPU tensor."""
+    if not host:
+        return _ptr(t, dtype, name)
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def layer_weights(cfg, w_dkv, w_uq, w_uk, w_uv, w_o, w_dq=None):
+    """mla_layer_weights for device weight tensors (kept alive by the caller)."""
+    dt = _tdtype(cfg)
+    return LayerWeights(int(w_o.shape[1]), int(w_dq.shape[1]) if w_dq is not None else 0,
+                        _ptr(w_dkv, dt, "w_dkv"), _ptr(w_dq, dt, "w_dq"), _ptr(w_uq, dt, "w_uq"),
+                        _ptr(w_uk, dt, "w_uk"), _ptr(w_uv, dt, "w_uv"), _ptr(w_o, dt, "w_o"))
+
+
+def layer_decode_step_workspace_size(cfg, weights, batch, max_blocks):
+    n = ctypes.c_size_t(0)
+    _check(lib().mla_layer_decode_step_workspace_size(ctypes.byref(cfg), ctypes.byref(weights),
+                                                       batch, max_blocks, ctypes.byref(n)),
+           "mla_layer_decode_step_workspace_size")
+    return n.value
+
+
+def layer_decode_step(cfg, weights, x, seq_lens, cache, block_table, out, io_flags=0,
+                      workspace=None, stream=None):
+    """mla_layer_decode_step: one full decode step (append, query, attention, W_O)."""
+    dt = _tdtype(cfg)
+    hin, hout = bool(io_flags & IO_HOST_INPUTS), bool(io_flags & IO_HOST_OUTPUT)
+    batch, max_blocks = block_table.shape
+    if workspace is None:
+        workspace = torch.empty(layer_decode_step_workspace_size(cfg, weights, batch, max_blocks),
+                                dtype=torch.uint8, device=cache.device)
+    rc = lib().mla_layer_decode_step(
+        ctypes.byref(cfg), ctypes.byref(weights), _ptr_io(x, dt, "x", hin),
+        _ptr_io(seq_lens, torch.int32, "seq_lens", hin), batch, _ptr(cache, dt, "cache"),
+        cache.shape[0], _ptr_io(block_table, torch.int32, "block_table", hin), max_blocks,
+        _ptr_io(out, dt, "out", hout), int(io_flags), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "mla_layer_decode_step")
+
+
+def cached_decode_step_workspace_size(cfg, batch, max_blocks):
+    n = ctypes.c_size_t(0)
+    _check(lib().mla_cached_decode_step_workspace_size(ctypes.byref(cfg), batch, max_blocks,
+                                                        ctypes.byref(n)),
+           "mla_cached_decode_step_workspace_size")
+    return n.value
+
+
+def cached_decode_step(cfg, q_nope, q_pe, w_uk, w_uv, seq_lens, cache, block_table, o_v,
+                       o_lat=None, lse=None, io_flags=0, workspace=None, stream=None):
+    """mla_cached_decode_step: absorb, attention and value projection in one call."""
+    dt = _tdtype(cfg)
+    hin, hout = bool(io_flags & IO_HOST_INPUTS), bool(io_flags & IO_HOST_OUTPUT)
+    batch, max_blocks = block_table.shape
+    if workspace is None:
+        workspace = torch.empty(cached_decode_step_workspace_size(cfg, batch, max_blocks),
+                                dtype=torch.uint8, device=cache.device)
+    rc = lib().mla_cached_decode_step(
+        ctypes.byref(cfg), _ptr_io(q_nope, dt, "q_nope", hin), _ptr_io(q_pe, dt, "q_pe", hin),
+        _ptr(w_uk, dt, "w_uk"), _ptr(w_uv, dt, "w_uv"),
+        _ptr_io(seq_lens, torch.int32, "seq_lens", hin), batch, _ptr(cache, dt, "cache"),
+        cache.shape[0], _ptr_io(block_table, torch.int32, "block_table", hin), max_blocks,
+        _ptr_io(o_v, dt, "o_v", hout), _ptr(o_lat, dt, "o_lat"), _ptr(lse, torch.float32, "lse"),
+        int(io_flags), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "mla_cached_decode_step")

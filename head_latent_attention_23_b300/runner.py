@@ -9,6 +9,11 @@ Step for a workload whose cache rows are given (shared-cache decode):
 Step for a workload driven by hidden states x (full layer):
     mla_query_proj -> mla_append_latent -> mla_absorb_q -> mla_decode
     -> mla_project_out (with W_O)
+
+``run_fused()`` issues the same step as one library call
+(mla_cached_decode_step, or mla_layer_decode_step when each sequence gets one
+new token), optionally with the per-step inputs and the result in pinned host
+memory.
 """
 import torch
 
@@ -61,6 +66,22 @@ class DecodeStep:
         self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
         self.o_v = torch.empty((B, H, c["d_v"]), dtype=dt, device=dev)
         self.workspace = mla.decode_workspace(self.cfg, B, dev)
+        maxb = self.block_table.shape[1]
+        # one library call per step: the shared-cache step, or the full layer
+        # step when each sequence gets exactly one new token (its newest)
+        self.fused = self.kind == "cached" or (
+            w["x_new"].shape[0] == B and torch.equal(w["x_new"], w["x_q"]) and
+            torch.equal(w["seq_idx_new"], torch.arange(B, dtype=torch.int32)) and
+            torch.equal(w["pos_new"], w["seq_lens"] - 1))
+        if self.kind == "cached":
+            n = mla.cached_decode_step_workspace_size(self.cfg, B, maxb)
+        elif self.fused:
+            self.weights = mla.layer_weights(self.cfg, self.w_dkv, self.w_uq, self.w_uk,
+                                             self.w_uv, self.w_o, w_dq=self.w_dq)
+            n = mla.layer_decode_step_workspace_size(self.cfg, self.weights, B, maxb)
+        else:
+            n = 0
+        self.step_ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
 
     # the graded core: split-KV attention + combine
     def decode(self, stream=None):
@@ -80,6 +101,29 @@ class DecodeStep:
                             stream)
         else:
             mla.project_out(self.cfg, self.o_lat, self.w_uv, self.o_v, stream=stream)
+
+    def run_fused(self, io_flags=0, inputs=None, result=None, stream=None):
+        """The step as one library call.  With io_flags, `inputs` (dict of
+        pinned host tensors: q_nope, q_pe or x; seq_lens; block_table) and
+        `result` (pinned host tensor for o_v or out) replace the device ones."""
+        if not self.fused:
+            raise ValueError("this workload appends several rows per sequence; use run()")
+        t = dict(q_nope=self.q_nope, q_pe=self.q_pe, seq_lens=self.seq_lens,
+                 block_table=self.block_table)
+        if self.kind == "token":
+            t["x"] = self.x_q
+        if inputs:
+            t.update(inputs)
+        if self.kind == "cached":
+            mla.cached_decode_step(self.cfg, t["q_nope"], t["q_pe"], self.w_uk, self.w_uv,
+                                   t["seq_lens"], self.cache, t["block_table"],
+                                   self.o_v if result is None else result, o_lat=self.o_lat,
+                                   lse=self.lse, io_flags=io_flags, workspace=self.step_ws,
+                                   stream=stream)
+        else:
+            mla.layer_decode_step(self.cfg, self.weights, t["x"], t["seq_lens"], self.cache,
+                                  t["block_table"], self.out if result is None else result,
+                                  io_flags=io_flags, workspace=self.step_ws, stream=stream)
 
     def kernels_per_step(self):
         """Kernel launches one run() issues."""

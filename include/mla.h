@@ -232,6 +232,87 @@ int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, co
                    void* scratch, size_t scratch_bytes, mla_stream_t stream);
 
 /*
+ * Whole decode steps in one call.  Each issues, on `stream`, every kernel of
+ * one step in the order of section 03 of "How DeepSeek Rewrote the
+ * Transformer (MLA)" (queries, scores against the cached rows, softmax,
+ * weighted sum, stack the heads and multiply by W_O), in latent space as the
+ * two merges of "Multi-Head Latent Attention (MLA)" allow, with the newest
+ * token's cache row appended first (section 04: the step reads every earlier
+ * row and adds one).  The intermediate tensors live in the caller's
+ * workspace.
+ *
+ * io_flags: MLA_IO_HOST_INPUTS means the per-step inputs (x or q_nope / q_pe,
+ * seq_lens and block_table) are pinned host memory and are copied to the
+ * workspace on `stream` before the first kernel; MLA_IO_HOST_OUTPUT means
+ * the result (out or o_v) is pinned host memory written by a copy after the
+ * last kernel.  Without the flags every pointer is device memory.  Weights
+ * and the cache are always device memory.
+ */
+#define MLA_IO_HOST_INPUTS 1
+#define MLA_IO_HOST_OUTPUT 2
+
+/*
+ * Weights of one MLA layer (device memory, dtype of the config, [in][out]):
+ *   w_dkv  [d_model][d_latent + d_rope]      [W_L | W_KR], the cache row of x
+ *   w_dq   [d_model][d_lq] or NULL            query compression W_LQ
+ *   w_uq   [d_q][heads][d_nope + d_rope]      per head [W_LQQ_h | W_QR_h],
+ *                                             d_q = d_lq, or d_model without w_dq
+ *   w_uk   [heads][d_latent][d_nope]          W_LK_h
+ *   w_uv   [heads][d_latent][d_v]             W_LV_h
+ *   w_o    [heads * d_v][d_model]             W_O
+ */
+typedef struct mla_layer_weights {
+    int d_model;
+    int d_lq;
+    const void* w_dkv;
+    const void* w_dq;
+    const void* w_uq;
+    const void* w_uk;
+    const void* w_uv;
+    const void* w_o;
+} mla_layer_weights;
+
+/*
+ * Full decode step of one layer for one new token per sequence:
+ *   row b of the cache at position seq_lens[b] - 1 = [x_b W_L | RoPE(x_b W_KR)]
+ *   (mla_append_latent), the query of x_b at the same position
+ *   (mla_query_proj), q_lat (mla_absorb_q), attention over rows
+ *   0 .. seq_lens[b] - 1 (mla_decode), out_b = concat_h(o_lat W_LV_h) W_O
+ *   (mla_project_out).
+ *   x         [batch][d_model]   hidden state of each sequence's new token
+ *   seq_lens  [batch] int32      tokens including the new one, >= 1
+ *   cache     [num_blocks][block_size][d_latent + d_rope]  (new rows written)
+ *   out       [batch][d_model]   (written)
+ *   workspace >= mla_layer_decode_step_workspace_size() bytes, 256-byte aligned
+ * Errors are those of the calls above; nothing is launched when host-side
+ * validation fails.
+ */
+int mla_layer_decode_step_workspace_size(const mla_config* cfg, const mla_layer_weights* w,
+                                         int batch, int max_blocks, size_t* bytes);
+int mla_layer_decode_step(const mla_config* cfg, const mla_layer_weights* w, const void* x,
+                          const int32_t* seq_lens, int batch, void* cache, int64_t num_blocks,
+                          const int32_t* block_table, int max_blocks, void* out, int io_flags,
+                          void* workspace, size_t ws_bytes, mla_stream_t stream);
+
+/*
+ * Decode step over a cache whose rows are given (no new row, no W_O):
+ * q_lat = q_nope W_LK_h^T (mla_absorb_q), attention (mla_decode) and
+ * o_v[b][h] = o_lat[b][h] W_LV_h (mla_project_out without W_O).
+ *   q_nope [batch][heads][d_nope], q_pe [batch][heads][d_rope]
+ *   o_v    [batch][heads][d_v]                     (written)
+ *   o_lat  [batch][heads][d_latent] or NULL         device, written when given
+ *   lse    [batch][heads] float32 or NULL           device, written when given
+ */
+int mla_cached_decode_step_workspace_size(const mla_config* cfg, int batch, int max_blocks,
+                                          size_t* bytes);
+int mla_cached_decode_step(const mla_config* cfg, const void* q_nope, const void* q_pe,
+                           const void* w_uk, const void* w_uv, const int32_t* seq_lens,
+                           int batch, const void* cache, int64_t num_blocks,
+                           const int32_t* block_table, int max_blocks, void* o_v, void* o_lat,
+                           float* lse, int io_flags, void* workspace, size_t ws_bytes,
+                           mla_stream_t stream);
+
+/*
  * mla_decode without a workspace argument: the split-KV partial results go to
  * a static device array of MLA_NOALLOC_SCRATCH_BYTES that the library itself
  * holds on every GPU that loads it, until the process exits.  The pages

@@ -78,3 +78,23 @@ def test_bad_sizes_and_null_pointers_are_rejected(L):
         mla.MLA_ERR_INVALID_ARG
     assert L.mla_query_proj(cp, None, 2, 16, None, 0, None, None, None, None, None, 0,
                             None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_step_calls_validate_on_the_host(L):
+    c = mla.config(128, 512, 64, 128, 128, 64, "bf16")
+    cp = ctypes.byref(c)
+    n = ctypes.c_size_t(0)
+    wts = mla.LayerWeights(0, 0, None, None, None, None, None, None)
+    assert L.mla_layer_decode_step_workspace_size(cp, ctypes.byref(wts), 4, 8, ctypes.byref(n)) == \
+        mla.MLA_ERR_INVALID_ARG
+    assert L.mla_layer_decode_step_workspace_size(cp, None, 4, 8, ctypes.byref(n)) == \
+        mla.MLA_ERR_INVALID_ARG
+    assert L.mla_layer_decode_step(cp, ctypes.byref(wts), None, None, 4, None, 1, None, 8, None,
+                                   0, None, 0, None) == mla.MLA_ERR_INVALID_ARG
+    assert L.mla_cached_decode_step_workspace_size(cp, 0, 8, ctypes.byref(n)) == \
+        mla.MLA_ERR_INVALID_ARG
+    # unknown io flag bits and null inputs are refused before any CUDA call
+    assert L.mla_cached_decode_step(cp, None, None, None, None, None, 4, None, 1, None, 8, None,
+                                    None, None, 4, None, 0, None) == mla.MLA_ERR_INVALID_ARG
+    assert L.mla_cached_decode_step(cp, None, None, None, None, None, 4, None, 1, None, 8, None,
+                                    None, None, 0, None, 0, None) == mla.MLA_ERR_INVALID_ARG

@@ -100,23 +100,33 @@ def test_masked_slots_do_not_leak():
     assert np.array_equal(o1, host(b.o_lat))
 
 
-def test_append_indexing_is_bit_exact():
+@pytest.mark.parametrize("max_pos", [256, 100000])
+def test_append_indexing_is_bit_exact(max_pos):
     """The append's rows scattered by the oracle's index map reproduce the GPU
-    cache byte for byte; every other slot keeps its canary."""
+    cache byte for byte; every other slot keeps its canary.  Positions up to
+    100,000 exercise the rotary angles of the long-context workloads."""
     for dtype, tol in (("bf16", TOL["bf16"]), ("f32", TOL["f32"])):
         g = torch.Generator().manual_seed(3)
         cfg = mla.config(128, 512, 64, 128, 128, 64, dtype)
         td = W.torch_dtype(dtype)
-        nb, B, maxb, n_tok, d_in = 12, 3, 4, 40, 320
-        bt = torch.randperm(nb, generator=g)[:B * maxb].reshape(B, maxb).to(torch.int32)
+        B, n_tok, d_in = 3, 40, 320
+        maxb = (max_pos + 63) // 64
         seq_idx = torch.randint(0, B, (n_tok,), generator=g).to(torch.int32)
-        pos = torch.randint(0, maxb * 64, (n_tok,), generator=g).to(torch.int32)
+        pos = torch.randint(0, max_pos, (n_tok,), generator=g).to(torch.int32)
         # distinct (seq, pos) so no two tokens target the same slot
-        key = seq_idx.long() * 100000 + pos.long()
+        key = seq_idx.long() * 1000000 + pos.long()
         keep = torch.unique(key, return_inverse=False)
-        seq_idx = (keep // 100000).to(torch.int32)
-        pos = (keep % 100000).to(torch.int32)
+        seq_idx = (keep // 1000000).to(torch.int32)
+        pos = (keep % 1000000).to(torch.int32)
         n_tok = seq_idx.numel()
+        # a page per (sequence, page index) that some token uses, in a permuted
+        # pool; the table's other entries point at pages no token writes
+        used = sorted({(int(b), int(p) // 64) for b, p in zip(seq_idx, pos)})
+        nb = len(used) + 4
+        ids = torch.randperm(nb, generator=g)
+        bt = torch.full((B, maxb), int(ids[-1]), dtype=torch.int32)
+        for i, (b, pg) in enumerate(used):
+            bt[b, pg] = int(ids[i])
         x = torch.randn(n_tok, d_in, generator=g).to(td)
         w_dkv = (torch.randn(d_in, 576, generator=g) / d_in ** 0.5).to(td)
         canary = torch.full((nb, 64, 576), 7.25, dtype=td)
@@ -191,6 +201,60 @@ def test_split_ranges_crossing_sequences_all_pairs():
     ref = O.reference_cached_decode(W.oracle_view(w))
     assert rel(host(o_lat), ref["o_lat"]) <= TOL["bf16"]
     assert rel(host(lse), ref["lse"]) <= TOL["bf16"]
+
+
+def _host_pinned(t):
+    return t.cpu().pin_memory()
+
+
+def test_layer_decode_step_single_call_matches_oracle():
+    """mla_layer_decode_step (one call: query projection, append of each
+    sequence's newest row, absorb, decode, W_LV and W_O) on a small full
+    layer (hidden 1024, query latent 256, DeepSeek-V2 head and latent widths,
+    batch 4, contexts 300), all outputs against the oracle; the host-buffer
+    form of the call returns the same bytes as the device form."""
+    w = W.token_decode(4, 300, seed=17, d_model=1024, d_lq=256, permute=True)
+    step = DecodeStep(w)
+    assert step.fused
+    step.run_fused()
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK
+    ref = O.reference_token_decode(W.oracle_view(w))
+    assert rel(host(step.out), ref["out"]) <= TOL["bf16"]
+    got = host(step.cache).reshape(-1, 576)
+    v = W.oracle_view(w)
+    rows = O.latent_rows(v["x_new"], v["w_dkv"], 512, 64, v["pos_new"])
+    for b in range(4):
+        pg = int(v["block_table"][b, 299 // 64])
+        assert rel(got[pg * 64 + 299 % 64], rows[b]) <= TOL["bf16"]
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    inputs = dict(x=_host_pinned(step.x_q), seq_lens=_host_pinned(step.seq_lens),
+                  block_table=_host_pinned(step.block_table))
+    step.run_fused(io_flags=mla.IO_HOST_INPUTS | mla.IO_HOST_OUTPUT, inputs=inputs, result=out_h)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK
+    assert torch.equal(out_h, step.out.cpu())
+
+
+def test_cached_decode_step_single_call_matches_oracle():
+    """mla_cached_decode_step (absorb, decode, W_LV in one call) against the
+    oracle, ragged lengths with permuted pages; host-buffer form equal to the
+    device form."""
+    w = W.cached_decode(3, [129, 1, 900], seed=19, permute=True)
+    step = DecodeStep(w)
+    step.run_fused()
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK
+    ref = O.reference_cached_decode(W.oracle_view(w))
+    res = step.results()
+    for key in ("o_lat", "o_v", "lse"):
+        assert rel(host(res[key]), ref[key]) <= TOL["bf16"], key
+    o_h = torch.empty(step.o_v.shape, dtype=step.o_v.dtype).pin_memory()
+    inputs = {k: _host_pinned(getattr(step, k)) for k in ("q_nope", "q_pe", "seq_lens",
+                                                          "block_table")}
+    step.run_fused(io_flags=mla.IO_HOST_INPUTS | mla.IO_HOST_OUTPUT, inputs=inputs, result=o_h)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, step.o_v.cpu())
 
 
 def test_invalid_block_id_is_flagged_not_read():
