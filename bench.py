@@ -348,8 +348,22 @@ def run_ours(args):
     rem = K - (K // G) * G
     dec_ev = [(torch.cuda.Event(enable_timing=True, external=True),
                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(G)]
-    graph_a = capture(ga_steps, dec_ev)
-    graph_b = capture([steps[i % R] for i in range(rem)], None) if rem else None
+    # A full-layer step is timed as the one library call a user makes
+    # (mla_layer_decode_step, whose batch-1 projections split K over all SMs);
+    # its mla_decode durations come from a replay of the same step issued as
+    # separate calls with events around mla_decode, right after the timed
+    # region.  Shared-cache steps issue the same kernels either way and are
+    # timed as separate calls with the events inside.
+    fused_timing = steps[0].kind == "token" and steps[0].fused
+    if fused_timing:
+        graph_a = capture(ga_steps, None, fused=True)
+        graph_b = capture([steps[i % R] for i in range(rem)], None, fused=True) if rem else None
+        graph_d = capture(ga_steps[:min(G, 100)], dec_ev[:min(G, 100)])
+        dec_ev = dec_ev[:min(G, 100)]
+    else:
+        graph_a = capture(ga_steps, dec_ev)
+        graph_b = capture([steps[i % R] for i in range(rem)], None) if rem else None
+        graph_d = None
     for _ in range(2):           # graph warm-up (first replays upload the graph)
         graph_a.replay()
     torch.cuda.synchronize()
@@ -369,7 +383,11 @@ def run_ours(args):
         dist.barrier()
     # tokens of all ranks over the slowest rank's time
     value, total_ms = job_rate(start.elapsed_time(end), B * K, dev)
-    # the last replay of graph A: one duration per mla_decode call
+    if graph_d is not None:
+        graph_d.replay()
+        graph_d.replay()
+        torch.cuda.synchronize()
+    # the last replay of graph A (or D): one duration per mla_decode call
     dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
     assert mla.get_status() == mla.MLA_OK, "device status after timed region"
 
@@ -430,10 +448,12 @@ def run_ours(args):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * steps[0].kernels_per_step(),
+        "gpu_launches": K * steps[0].kernels_per_step(fused=fused_timing),
         "timing": (f"CUDA graphs of {G} steps replayed {K // G} times"
                    + (f" + one of {rem} steps" if rem else "")
-                   + "; mla_decode durations from events inside the last replay"),
+                   + ("; each step one mla_layer_decode_step call; mla_decode durations from "
+                      "events in a replay of the step as separate calls" if fused_timing else
+                      "; mla_decode durations from events inside the last replay")),
         "clocks": clk.summary(),
     }
     print(json.dumps(out), flush=True)
@@ -441,9 +461,10 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def capture(step_list, ev_pairs):
+def capture(step_list, ev_pairs, fused=False):
     """A CUDA graph of the given steps' library calls, in order; with
-    ev_pairs, timing events around each mla_decode call."""
+    ev_pairs, timing events around each mla_decode call; with fused, each step
+    as its one whole-step library call."""
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -452,7 +473,10 @@ def capture(step_list, ev_pairs):
         with torch.cuda.graph(g, stream=side):
             cs = torch.cuda.current_stream()
             for j, s in enumerate(step_list):
-                _run_with_decode_events(s, ev_pairs[j] if ev_pairs else None, cs)
+                if fused:
+                    s.run_fused()
+                else:
+                    _run_with_decode_events(s, ev_pairs[j] if ev_pairs else None, cs)
     torch.cuda.current_stream().wait_stream(side)
     return g
 

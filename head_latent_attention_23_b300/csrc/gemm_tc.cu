@@ -9,9 +9,16 @@
 // 128 x 128 tiles of C, K in 64-deep slices of A (K-major) and B (K-major or
 // N-major) streamed into a 4-stage ring with TMA (128-byte swizzle);
 // tcgen05.mma (M=128, N=128, K=16) accumulates in TMEM.  The kernel is
-// persistent (at most one CTA per SM, looping over tiles) so that, at decode
-// batch sizes where a tile is a few k slices, the weight stream never stops
-// for a CTA's set-up or epilogue.
+// persistent (at most one CTA per SM, looping over work items) so that, at
+// decode batch sizes where a tile is a few k slices, the weight stream never
+// stops for a CTA's set-up or epilogue.
+//
+// Split-K.  A product with fewer output tiles than SMs (W_O, the query and
+// cache down-projections at decode batch sizes) would leave most SMs idle
+// while a few stream long K ranges.  With p.splits > 1 a work item is a
+// (tile, K range) pair; its epilogue writes an fp32 partial tile to
+// p.partial[split][m][n], and splitk_reduce_kernel adds the partials and
+// applies the product's epilogue (store, or RoPE and the paged scatter).
 #include "kernels.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -40,13 +47,22 @@ __device__ __forceinline__ TileId tile_of(int t, int tiles_n, int tiles_m) {
     return r;
 }
 
-// Persistent: CTA c takes tiles c, c + gridDim.x, ...  Warp 0 streams the k
-// slices of all its tiles through one ring; one thread of warp 1 accumulates
-// each tile into one of two TMEM buffers; warps 2-5 drain a finished buffer
-// (128 rows = TMEM lanes) while the next tile is being computed.
+// Persistent: CTA c takes work items c, c + gridDim.x, ...  Warp 0 streams
+// the k slices of all its items through one ring; one thread of warp 1
+// accumulates each item into one of two TMEM buffers; warps 2-5 drain a
+// finished buffer (128 rows = TMEM lanes) while the next item is computed.
+// Item i is tile i / splits, K range i % splits.
+__device__ __forceinline__ void item_range(int item, int splits, int nk, int* tile, int* kt0,
+                                           int* kt1) {
+    const int sp = item % splits;
+    *tile = item / splits;
+    *kt0 = (int)((int64_t)sp * nk / splits);
+    *kt1 = (int)((int64_t)(sp + 1) * nk / splits);
+}
+
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
-                   const TcGemmParams p, int tiles_n, int tiles_m, int num_tiles) {
+                   const TcGemmParams p, int tiles_n, int tiles_m, int num_items) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
@@ -93,9 +109,11 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const TileId ti = tile_of(t, tiles_n, tiles_m);
-                for (int kt = 0; kt < nk; ++kt, ++it) {
+            for (int t = blockIdx.x; t < num_items && ok; t += gridDim.x) {
+                int tile, kt0, kt1;
+                item_range(t, p.splits, nk, &tile, &kt0, &kt1);
+                const TileId ti = tile_of(tile, tiles_n, tiles_m);
+                for (int kt = kt0; kt < kt1; ++kt, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait_fast(&empty[s], ((it / kStages) & 1) ^ 1, abort_flag,
                                         p.status)) {
@@ -122,28 +140,34 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t idesc = idesc_bf16(kBM, kBN, false, p.b_mn != 0);
             int it = 0, lt = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++lt) {
+            // descriptors advance by the k step: 32 bytes (2) along K for a
+            // K-major operand, 16 rows (2048 bytes, 128) for an N-major B
+            const uint64_t bstep = p.b_mn ? 128 : 2;
+            for (int t = blockIdx.x; t < num_items && ok; t += gridDim.x, ++lt) {
+                int tile, kt0, kt1;
+                item_range(t, p.splits, nk, &tile, &kt0, &kt1);
                 const int ab = lt % kAcc;
                 if (!mbar_wait_fast(&acc_empty[ab], ((lt / kAcc) & 1) ^ 1, abort_flag, p.status))
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(ab * kBN);
-                for (int kt = 0; kt < nk; ++kt, ++it) {
+                for (int kt = kt0; kt < kt1; ++kt, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait_fast(&full[s], (it / kStages) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + s * kTileBytes);
-                    const uint32_t b0 = smem_u32(sB + s * kTileBytes);
+                    const uint64_t ad = sdesc(smem_u32(sA + s * kTileBytes), 16, 1024, 2);
+                    const uint64_t bd = p.b_mn
+                                            ? sdesc(smem_u32(sB + s * kTileBytes), kTileBytes / 2, 1024, 2)
+                                            : sdesc(smem_u32(sB + s * kTileBytes), 16, 1024, 2);
+                    mma_ss(d, ad, bd, idesc, kt != kt0);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        const uint64_t ad = sdesc(a0 + 32 * k, 16, 1024, 2);
-                        const uint64_t bd = p.b_mn ? sdesc(b0 + 2048 * k, kTileBytes / 2, 1024, 2)
-                                                   : sdesc(b0 + 32 * k, 16, 1024, 2);
-                        mma_ss(d, ad, bd, idesc, (kt | k) != 0);
-                    }
+                    for (int k = 1; k < kBK / 16; ++k)
+                        asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d),
+                                     "l"(ad + 2 * k), "l"(bd + bstep * k), "r"(idesc)
+                                     : "memory");
                     tc_commit(&empty[s]);
                 }
                 if (!ok) break;
@@ -158,9 +182,12 @@ __global__ void __launch_bounds__(192, 1)
         const int q = warp & 3;
         const int row = q * 32 + lane;
         int lt = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
+        for (int t = blockIdx.x; t < num_items; t += gridDim.x, ++lt) {
+            int tile, kt0, kt1;
+            item_range(t, p.splits, nk, &tile, &kt0, &kt1);
+            const int split = t % p.splits;
             const int ab = lt % kAcc;
-            const TileId ti = tile_of(t, tiles_n, tiles_m);
+            const TileId ti = tile_of(tile, tiles_n, tiles_m);
             const int n0 = ti.n0, z = ti.z;
             const int m = ti.m0 + row;
             bool ok = mbar_wait_fast(&acc_full[ab], (lt / kAcc) & 1, abort_flag, p.status);
@@ -168,7 +195,7 @@ __global__ void __launch_bounds__(192, 1)
             if (!ok) break;
             tc_fence_after();
             int64_t slot = -1;
-            if (p.epi == 1 && m < p.M) {
+            if (p.splits == 1 && p.epi == 1 && m < p.M) {
                 const int b = p.seq_idx[m], ps = p.pos[m];
                 if (b >= 0 && b < p.batch && ps >= 0 && ps < p.max_blocks * p.block_size) {
                     const int32_t blk = p.block_table[(size_t)b * p.max_blocks + ps / p.block_size];
@@ -188,7 +215,18 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
                 const int nb = n0 + c;
-                if (p.epi == 1) {
+                if (p.splits > 1) {
+                    // fp32 partial of this K range; splitk_reduce_kernel finishes
+                    float* P = p.partial + ((size_t)split * p.M + m) * p.N + nb;
+                    if (nb + 16 <= p.N) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *(float4*)(P + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    } else {
+                        for (int i = 0; i < 16; ++i)
+                            if (nb + i < p.N) P[i] = v[i];
+                    }
+                } else if (p.epi == 1) {
                     if (nb >= p.N) continue;
                     if (nb >= p.d_latent) {
                         const int ps = p.pos[m];
@@ -249,10 +287,88 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 1) tmem_dealloc(tmem, kAcc * kBN);
 }
 
+// Sum of the split-K partials and the product's epilogue: thread = four
+// consecutive columns of one row.  Same arithmetic as the one-pass epilogue
+// of gemm_tc_kernel (fp32 sums, one rounding to the output type; RoPE angles
+// in fp64), so a split changes only the order of the fp32 additions.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcGemmParams p) {
+    pdl_wait_primary();
+    const int n4 = p.N / 4;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx < (int64_t)p.M * n4) {
+        const int m = (int)(idx / n4), n = (int)(idx % n4) * 4;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int sp = 0; sp < p.splits; ++sp) {
+            const float4 x = *(const float4*)(p.partial + ((size_t)sp * p.M + m) * p.N + n);
+            v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+        }
+        if (p.epi == 1) {
+            int64_t slot = -1;
+            const int b = p.seq_idx[m], ps = p.pos[m];
+            if (b >= 0 && b < p.batch && ps >= 0 && ps < p.max_blocks * p.block_size) {
+                const int32_t blk = p.block_table[(size_t)b * p.max_blocks + ps / p.block_size];
+                if (blk >= 0 && blk < p.num_blocks)
+                    slot = (int64_t)blk * p.block_size + ps % p.block_size;
+            }
+            if (slot < 0 && n == 0) flag(p.status, MLA_ERR_INDEX);
+            if (n >= p.d_latent) {
+#pragma unroll
+                for (int i = 0; i < 4; i += 2) {
+                    const int j = (n + i - p.d_latent) / 2;
+                    const double theta = pow(p.rope_base, -2.0 * j / (double)p.d_rope);
+                    const double phi = fmod((double)ps * theta, 6.283185307179586476925286766559);
+                    double sn, cs;
+                    sincos(phi, &sn, &cs);
+                    const float x0 = v[i], x1 = v[i + 1];
+                    v[i] = x0 * (float)cs - x1 * (float)sn;
+                    v[i + 1] = x0 * (float)sn + x1 * (float)cs;
+                }
+            }
+            uint2 w;
+            w.x = pack_bf16(v[0], v[1]);
+            w.y = pack_bf16(v[2], v[3]);
+            if (slot >= 0) *(uint2*)(p.cache + slot * p.N + n) = w;
+            if (p.dense_out) *(uint2*)(p.dense_out + (size_t)m * p.N + n) = w;
+        } else if (p.c_dtype == MLA_DTYPE_BF16) {
+            uint2 w;
+            w.x = pack_bf16(v[0], v[1]);
+            w.y = pack_bf16(v[2], v[3]);
+            *(uint2*)((__nv_bfloat16*)p.C + (int64_t)m * p.sCm + n) = w;
+        } else {
+            *(float4*)((float*)p.C + (int64_t)m * p.sCm + n) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    }
+    pdl_launch_dependents();
+}
+
+// Number of K ranges for a product of `tiles` output tiles and `nk` k
+// slices on `sms` SMs: the smallest count that keeps at least 85% of the
+// SMs' item slots busy (items = tiles x splits, in waves of `sms`), with at
+// least four k slices per range and partials that fit the scratch.
+int choose_splits(int64_t tiles, int nk, int sms, size_t bytes_per_split, size_t scratch) {
+    if (tiles <= 0 || scratch < bytes_per_split * 2) return 1;
+    const int max_s = nk / 4 < 32 ? nk / 4 : 32;
+    for (int s = 1; s <= max_s; ++s) {
+        if ((size_t)s * bytes_per_split > scratch) return s > 1 ? s - 1 : 1;
+        const double waves = (double)(tiles * s) / sms;
+        if (waves / ceil(waves) >= 0.85) return s;
+    }
+    return max_s > 1 ? max_s : 1;
+}
+
 }  // namespace
 
-cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmParams& p,
+size_t gemm_tc_split_scratch(int M, int N, int K, int sms) {
+    if (M <= 0 || N <= 0 || K <= 0 || N % 4) return 0;
+    const int64_t tiles = (int64_t)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
+    const size_t per = (size_t)M * N * sizeof(float);
+    const int s = choose_splits(tiles, (K + kBK - 1) / kBK, sms, per, (size_t)-1 / 2);
+    return s > 1 ? (size_t)s * per : 0;
+}
+
+cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmParams& pin,
                            int batch, cudaStream_t st) {
+    TcGemmParams p = pin;
     if (p.M <= 0 || p.N <= 0 || p.K <= 0 || batch <= 0) return cudaErrorInvalidValue;
     CUtensorMap ta, tb;
     const uint32_t boxA[3] = {64, 128, 1};
@@ -278,8 +394,14 @@ cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmP
         return cudaErrorInvalidDevice;
     const int tiles_n = (p.N + kBN - 1) / kBN, tiles_m = (p.M + kBM - 1) / kBM;
     const int64_t tiles = (int64_t)tiles_n * tiles_m * batch;
-    if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
-    const int grid = (int)(tiles < sms[dev] ? tiles : sms[dev]);
+    const int nk = (p.K + kBK - 1) / kBK;
+    p.splits = 1;
+    if (batch == 1 && p.partial && p.N % 4 == 0 && ((uintptr_t)p.partial & 15) == 0)
+        p.splits = choose_splits(tiles, nk, sms[dev], (size_t)p.M * p.N * sizeof(float),
+                                 p.partial_bytes);
+    const int64_t items = tiles * p.splits;
+    if (items > 0x7fffffff) return cudaErrorInvalidValue;
+    const int grid = (int)(items < sms[dev] ? items : sms[dev]);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(192);
@@ -290,7 +412,17 @@ cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmP
     la[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = la;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, ta, tb, p, tiles_n, tiles_m, (int)tiles);
+    cudaError_t e =
+        cudaLaunchKernelEx(&cfg, gemm_tc_kernel, ta, tb, p, tiles_n, tiles_m, (int)items);
+    if (e != cudaSuccess || p.splits == 1) return e;
+    const int64_t threads = (int64_t)p.M * (p.N / 4);
+    cudaLaunchConfig_t rc = {};
+    rc.gridDim = dim3((unsigned)((threads + 255) / 256));
+    rc.blockDim = dim3(256);
+    rc.stream = st;
+    rc.attrs = la;
+    rc.numAttrs = 1;
+    return cudaLaunchKernelEx(&rc, splitk_reduce_kernel, p);
 }
 
 }  // namespace mla

@@ -115,9 +115,17 @@ struct TcGemmParams {
     __nv_bfloat16* cache;
     __nv_bfloat16* dense_out;
     int* status;
+    // split-K (batch-1 products only): fp32 scratch for the partial tiles, or
+    // null to compute every tile in one pass; splits is chosen by the launcher
+    float* partial;
+    size_t partial_bytes;
+    int splits;
 };
 
 cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmParams& p,
                            int batch, cudaStream_t st);
+// fp32 scratch bytes with which launch_gemm_tc would split a batch-1 M x N x K
+// product over `sms` SMs (0: it would not split).
+size_t gemm_tc_split_scratch(int M, int N, int K, int sms);
 
 }  // namespace mla

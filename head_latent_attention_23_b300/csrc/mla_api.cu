@@ -101,11 +101,18 @@ TcOperand op3(const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s
     return o;
 }
 
+// fp32 scratch a projection may use for split-K partials (none: one pass)
+struct SplitScratch {
+    float* ptr = nullptr;
+    size_t bytes = 0;
+};
+
 TcGemmParams gemm_params(int M, int N, int K, bool b_mn, void* C, int64_t sCz, int64_t sCm,
-                         int c_dtype, int* status) {
+                         int c_dtype, int* status, SplitScratch sp = SplitScratch{}) {
     TcGemmParams g{};
     g.M = M; g.N = N; g.K = K; g.b_mn = b_mn ? 1 : 0; g.epi = 0;
     g.C = C; g.sCz = sCz; g.sCm = sCm; g.c_dtype = c_dtype; g.status = status;
+    g.partial = sp.ptr; g.partial_bytes = sp.bytes;
     return g;
 }
 
@@ -174,10 +181,14 @@ int mla_decode_path(const mla_config* cfg) {
     return use_tc(cfg, 1) ? 1 : 0;
 }
 
-int mla_append_latent(const mla_config* cfg, const void* x, int n_tok, int d_in,
+}  // extern "C"
+
+namespace {
+
+int append_latent_impl(const mla_config* cfg, const void* x, int n_tok, int d_in,
                       const void* w_dkv, const int32_t* seq_idx, const int32_t* pos,
                       const int32_t* block_table, int batch, int max_blocks, void* cache,
-                      int64_t num_blocks, void* dense_out, mla_stream_t stream) {
+                      int64_t num_blocks, void* dense_out, mla_stream_t stream, SplitScratch sp) {
     if (int rc = check_cfg(cfg)) return rc;
     if (n_tok < 0 || d_in < 1 || d_in > 65536 || batch < 1 || max_blocks < 1 ||
         num_blocks < 1)
@@ -195,7 +206,7 @@ int mla_append_latent(const mla_config* cfg, const void* x, int n_tok, int d_in,
         // rotary part and writes each row to its paged slot (and dense_out)
         TcOperand A = op3(x, d_in, n_tok, 1, (uint64_t)d_in * 2, (uint64_t)d_in * 2 * n_tok);
         TcOperand B = op3(w_dkv, D, d_in, 1, (uint64_t)D * 2, (uint64_t)D * 2 * d_in);
-        TcGemmParams g = gemm_params(n_tok, D, d_in, true, nullptr, 0, 0, MLA_DTYPE_BF16, status);
+        TcGemmParams g = gemm_params(n_tok, D, d_in, true, nullptr, 0, 0, MLA_DTYPE_BF16, status, sp);
         g.epi = 1;
         g.d_latent = cfg->d_latent; g.d_rope = cfg->d_rope; g.block_size = cfg->block_size;
         g.max_blocks = max_blocks; g.batch = batch; g.num_blocks = num_blocks;
@@ -211,6 +222,17 @@ int mla_append_latent(const mla_config* cfg, const void* x, int n_tok, int d_in,
     a.seq_idx = seq_idx; a.pos = pos; a.block_table = block_table; a.cache = cache;
     a.dense_out = dense_out; a.rows_f32 = nullptr; a.status = status;
     return cuda_rc(launch_append(a, cfg->dtype, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_append_latent(const mla_config* cfg, const void* x, int n_tok, int d_in,
+                      const void* w_dkv, const int32_t* seq_idx, const int32_t* pos,
+                      const int32_t* block_table, int batch, int max_blocks, void* cache,
+                      int64_t num_blocks, void* dense_out, mla_stream_t stream) {
+    return append_latent_impl(cfg, x, n_tok, d_in, w_dkv, seq_idx, pos, block_table, batch, max_blocks, cache, num_blocks, dense_out, stream, SplitScratch{});
 }
 
 int mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* w_uk, int batch,
@@ -291,8 +313,12 @@ int mla_decode_combine(const mla_config* cfg, const float* o_part, const float* 
                                         (cudaStream_t)stream));
 }
 
-int mla_project_out(const mla_config* cfg, const void* o_lat, const void* w_uv, int batch,
-                    void* o_v, const void* w_o, int d_model, void* out, mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int project_out_impl(const mla_config* cfg, const void* o_lat, const void* w_uv, int batch,
+                    void* o_v, const void* w_o, int d_model, void* out, mla_stream_t stream, SplitScratch sp) {
     if (int rc = check_cfg(cfg)) return rc;
     if (batch < 0 || (w_o && d_model < 1)) return MLA_ERR_INVALID_ARG;
     if (batch == 0) return MLA_OK;
@@ -316,7 +342,7 @@ int mla_project_out(const mla_config* cfg, const void* o_lat, const void* w_uv, 
         TcOperand A2 = op3(o_v, KO, batch, 1, KO * 2, KO * 2 * batch);
         TcOperand B2 = op3(w_o, d_model, KO, 1, (uint64_t)d_model * 2, KO * d_model * 2);
         TcGemmParams g2 = gemm_params(batch, d_model, (int)KO, true, out, 0, d_model,
-                                      MLA_DTYPE_BF16, status);
+                                      MLA_DTYPE_BF16, status, sp);
         return cuda_rc(launch_gemm_tc(A2, B2, g2, 1, st));
     }
     // per head h: o_v[:, h, :] (batch x DV) = o_lat[:, h, :] (batch x DL) . W_LV_h (DL x DV)
@@ -336,6 +362,15 @@ int mla_project_out(const mla_config* cfg, const void* o_lat, const void* w_uv, 
     return cuda_rc(launch_gemm_simt(o, cfg->dtype, cfg->dtype, cfg->dtype, st));
 }
 
+}  // namespace
+
+extern "C" {
+
+int mla_project_out(const mla_config* cfg, const void* o_lat, const void* w_uv, int batch,
+                    void* o_v, const void* w_o, int d_model, void* out, mla_stream_t stream) {
+    return project_out_impl(cfg, o_lat, w_uv, batch, o_v, w_o, d_model, out, stream, SplitScratch{});
+}
+
 int mla_query_proj_workspace_size(const mla_config* cfg, int batch, int d_lq, size_t* bytes) {
     if (int rc = check_cfg(cfg)) return rc;
     if (!bytes || batch < 1 || d_lq < 0) return MLA_ERR_INVALID_ARG;
@@ -344,9 +379,13 @@ int mla_query_proj_workspace_size(const mla_config* cfg, int batch, int d_lq, si
     return MLA_OK;
 }
 
-int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, const void* w_dq,
+}  // extern "C"
+
+namespace {
+
+int query_proj_impl(const mla_config* cfg, const void* x, int batch, int d_in, const void* w_dq,
                    int d_lq, const void* w_uq, const int32_t* pos, void* q_nope, void* q_pe,
-                   void* scratch, size_t scratch_bytes, mla_stream_t stream) {
+                   void* scratch, size_t scratch_bytes, mla_stream_t stream, SplitScratch sp) {
     if (int rc = check_cfg(cfg)) return rc;
     if (batch < 1 || d_in < 1 || (w_dq && d_lq < 1)) return MLA_ERR_INVALID_ARG;
     if (!x || !w_uq || !pos || !q_nope || (!q_pe && cfg->d_rope > 0)) return MLA_ERR_INVALID_ARG;
@@ -370,7 +409,7 @@ int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, co
             TcOperand B = op3(w_dq, d_lq, d_in, 1, (uint64_t)d_lq * 2,
                               (uint64_t)d_lq * 2 * d_in);
             TcGemmParams g = gemm_params(batch, d_lq, d_in, true, cq, 0, d_lq, MLA_DTYPE_BF16,
-                                         status);
+                                         status, sp);
             if (int rc = cuda_rc(launch_gemm_tc(A, B, g, 1, st))) return rc;
             a_in = cq;
             k_in = d_lq;
@@ -379,7 +418,7 @@ int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, co
         TcOperand A = op3(a_in, k_in, batch, 1, (uint64_t)k_in * 2, (uint64_t)k_in * 2 * batch);
         TcOperand B = op3(w_uq, NQ, k_in, 1, NQ * 2, NQ * 2 * k_in);
         TcGemmParams g = gemm_params(batch, (int)NQ, k_in, true, q_all, 0, (int64_t)NQ,
-                                     MLA_DTYPE_F32, status);
+                                     MLA_DTYPE_F32, status, sp);
         if (int rc = cuda_rc(launch_gemm_tc(A, B, g, 1, st))) return rc;
         return cuda_rc(launch_q_split_rope(q_all, batch, H, cfg->d_nope, cfg->d_rope, pos,
                                            cfg->rope_base, q_nope, q_pe, cfg->dtype, st));
@@ -404,6 +443,16 @@ int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, co
     if (int rc = cuda_rc(launch_gemm_simt(u, a_dtype, cfg->dtype, MLA_DTYPE_F32, st))) return rc;
     return cuda_rc(launch_q_split_rope(q_all, batch, H, cfg->d_nope, cfg->d_rope, pos,
                                        cfg->rope_base, q_nope, q_pe, cfg->dtype, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_query_proj(const mla_config* cfg, const void* x, int batch, int d_in, const void* w_dq,
+                   int d_lq, const void* w_uq, const int32_t* pos, void* q_nope, void* q_pe,
+                   void* scratch, size_t scratch_bytes, mla_stream_t stream) {
+    return query_proj_impl(cfg, x, batch, d_in, w_dq, d_lq, w_uq, pos, q_nope, q_pe, scratch, scratch_bytes, stream, SplitScratch{});
 }
 
 // ---------------------------------------------------------------------------
@@ -441,6 +490,7 @@ struct LayerWs {
     int32_t *seq_lens, *block_table, *pos, *seq_idx;
     void *x, *q_nope, *q_pe, *q_lat, *o_lat, *o_v, *out, *q_scratch, *dec;
     size_t q_scratch_bytes, dec_bytes;
+    SplitScratch split;   // split-K partials of the batch-1 projections
 };
 
 int layer_ws(const mla_config* c, const mla_layer_weights* w, int batch, int max_blocks,
@@ -466,6 +516,23 @@ int layer_ws(const mla_config* c, const mla_layer_weights* w, int batch, int max
     ws->q_scratch = k.take(qs);
     ws->dec_bytes = decode_ws_bytes(c, W, batch);
     ws->dec = k.take(ws->dec_bytes);
+    // the largest split-K scratch of the step's batch-1 products: W_DQ, W_UQ
+    // (query), W_DKV (cache row), W_O (output)
+    int sms;
+    if (int rc = num_sms(&sms)) return rc;
+    const int nh = c->heads, dq = c->d_nope + c->d_rope, D = c->d_latent + c->d_rope;
+    const int qin = w->w_dq ? w->d_lq : w->d_model;
+    size_t sb = 0;
+    auto upd = [&](int M, int N, int K) {
+        const size_t b = gemm_tc_split_scratch(M, N, K, sms);
+        if (b > sb) sb = b;
+    };
+    if (w->w_dq) upd(batch, w->d_lq, w->d_model);
+    upd(batch, nh * dq, qin);
+    upd(batch, D, w->d_model);
+    upd(batch, w->d_model, nh * c->d_v);
+    ws->split.bytes = sb;
+    ws->split.ptr = (float*)k.take(sb);
     *total = k.used;
     return MLA_OK;
 }
@@ -540,13 +607,13 @@ int mla_layer_decode_step(const mla_config* cfg, const mla_layer_weights* w, con
     if (launch_step_positions((const int32_t*)sl, batch, ws.pos, ws.seq_idx, st) != cudaSuccess)
         return MLA_ERR_CUDA;
     mla_stream_t s = stream;
-    if (int rc = mla_query_proj(cfg, xs, batch, w->d_model, w->w_dq, w->w_dq ? w->d_lq : 0,
-                                w->w_uq, ws.pos, ws.q_nope, ws.q_pe, ws.q_scratch,
-                                ws.q_scratch_bytes, s))
+    if (int rc = query_proj_impl(cfg, xs, batch, w->d_model, w->w_dq, w->w_dq ? w->d_lq : 0,
+                                 w->w_uq, ws.pos, ws.q_nope, ws.q_pe, ws.q_scratch,
+                                 ws.q_scratch_bytes, s, ws.split))
         return rc;
-    if (int rc = mla_append_latent(cfg, xs, batch, w->d_model, w->w_dkv, ws.seq_idx, ws.pos,
-                                   (const int32_t*)bt, batch, max_blocks, cache, num_blocks,
-                                   nullptr, s))
+    if (int rc = append_latent_impl(cfg, xs, batch, w->d_model, w->w_dkv, ws.seq_idx, ws.pos,
+                                    (const int32_t*)bt, batch, max_blocks, cache, num_blocks,
+                                    nullptr, s, ws.split))
         return rc;
     if (int rc = mla_absorb_q(cfg, ws.q_nope, w->w_uk, batch, ws.q_lat, s)) return rc;
     if (int rc = mla_decode(cfg, ws.q_lat, ws.q_pe, cache, num_blocks, (const int32_t*)bt,
@@ -554,7 +621,8 @@ int mla_layer_decode_step(const mla_config* cfg, const mla_layer_weights* w, con
                             ws.dec_bytes, s))
         return rc;
     void* o = hout ? ws.out : out;
-    if (int rc = mla_project_out(cfg, ws.o_lat, w->w_uv, batch, ws.o_v, w->w_o, w->d_model, o, s))
+    if (int rc = project_out_impl(cfg, ws.o_lat, w->w_uv, batch, ws.o_v, w->w_o, w->d_model, o, s,
+                                  ws.split))
         return rc;
     if (hout && cudaMemcpyAsync(out, ws.out, (size_t)batch * w->d_model * es,
                                 cudaMemcpyDeviceToHost, st) != cudaSuccess)

@@ -125,13 +125,42 @@ class DecodeStep:
                                   t["block_table"], self.out if result is None else result,
                                   io_flags=io_flags, workspace=self.step_ws, stream=stream)
 
-    def kernels_per_step(self):
-        """Kernel launches one run() issues."""
+    def kernels_per_step(self, fused=False):
+        """Kernel launches one run() (or, with fused, one run_fused()) issues.
+        The fused full-layer step adds the positions kernel and a split-K
+        reduction after each batch-1 projection that splits K."""
         n = 1 + 2 + 1                       # absorb, decode core + combine, o_v
         if self.kind == "token":
             n += (2 if self.w_dq is not None else 1) + 1   # query GEMM(s) + split/rope
             n += 1                          # append
             n += 1                          # W_O
+            if fused:
+                n += 1 + self.split_reductions()
+        return n
+
+    def split_reductions(self):
+        """Batch-1 projections of the fused full-layer step that the library
+        splits along K (each adds one reduction kernel), by the library's rule:
+        the fewest K ranges that keep 85% of the SMs' work slots busy."""
+        import math
+        sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        c, B = self.cfg_dict, self.B
+        d_model = self.out.shape[1]
+        prods = [(c["heads"] * (c["d_nope"] + c["d_rope"]), self.w_uq.shape[0]),
+                 (c["d_latent"] + c["d_rope"], d_model), (d_model, c["heads"] * c["d_v"])]
+        if self.w_dq is not None:
+            prods.append((self.w_dq.shape[1], d_model))
+        n = 0
+        for N, K in prods:
+            tiles = math.ceil(N / 128) * math.ceil(B / 128)
+            nk = math.ceil(K / 64)
+            best = 1
+            for s in range(1, min(nk // 4, 32) + 1):
+                waves = tiles * s / sms
+                best = s
+                if waves / math.ceil(waves) >= 0.85:
+                    break
+            n += best > 1
         return n
 
     def results(self):
