@@ -85,43 +85,57 @@ cudaError_t launch_append(const AppendArgs& a, int dtype, cudaStream_t st) {
 
 // ---------------------------------------------------------------- queries
 // q_all [batch][heads][d_nope + d_rope] fp32 -> q_nope (copy) and q_pe
-// (rotated at the sequence's position), both in dtype.
+// (rotated at the sequence's position), both in dtype.  One CTA per
+// sequence: the rotation angles depend only on the position, so each pair's
+// cosine and sine are formed once per sequence (in fp64, then rounded to
+// fp32) and shared by all heads; fp64 transcendentals are slow on this GPU.
 template <typename T>
-__global__ void q_split_rope_kernel(const float* __restrict__ q_all, int heads, int d_nope,
-                                    int d_rope, const int32_t* __restrict__ pos,
-                                    double rope_base, T* __restrict__ q_nope,
-                                    T* __restrict__ q_pe) {
-    const int b = blockIdx.x, h = blockIdx.y;
-    const int dq = d_nope + d_rope;
-    const float* src = q_all + ((size_t)b * heads + h) * dq;
-    T* dn = q_nope + ((size_t)b * heads + h) * d_nope;
-    T* dp = q_pe + ((size_t)b * heads + h) * d_rope;
-    for (int j = threadIdx.x; j < d_nope; j += blockDim.x) dn[j] = from_f<T>(src[j]);
+__global__ void __launch_bounds__(256) q_split_rope_kernel(
+    const float* __restrict__ q_all, int heads, int d_nope, int d_rope,
+    const int32_t* __restrict__ pos, double rope_base, T* __restrict__ q_nope,
+    T* __restrict__ q_pe) {
+    extern __shared__ float cs[];   // [d_rope / 2][2]: cos, sin
+    const int b = blockIdx.x, half_r = d_rope / 2;
     const int p = pos[b];
-    for (int j = threadIdx.x; j < d_rope / 2; j += blockDim.x) {
-        double theta = pow(rope_base, -2.0 * (double)j / (double)d_rope);
-        double phi = fmod((double)p * theta, 6.283185307179586476925286766559);
-        double sn, cs;
-        sincos(phi, &sn, &cs);
-        float c = (float)cs, s = (float)sn;
-        float x0 = src[d_nope + 2 * j], x1 = src[d_nope + 2 * j + 1];
-        dp[2 * j] = from_f<T>(x0 * c - x1 * s);
-        dp[2 * j + 1] = from_f<T>(x0 * s + x1 * c);
+    for (int j = threadIdx.x; j < half_r; j += blockDim.x) {
+        const double theta = pow(rope_base, -2.0 * (double)j / (double)d_rope);
+        const double phi = fmod((double)p * theta, 6.283185307179586476925286766559);
+        double sn, c;
+        sincos(phi, &sn, &c);
+        cs[2 * j] = (float)c;
+        cs[2 * j + 1] = (float)sn;
+    }
+    __syncthreads();
+    const int dq = d_nope + d_rope;
+    const float* src = q_all + (size_t)b * heads * dq;
+    T* dn = q_nope + (size_t)b * heads * d_nope;
+    T* dp = q_pe + (size_t)b * heads * d_rope;
+    for (int e = threadIdx.x; e < heads * d_nope; e += blockDim.x) {
+        const int h = e / d_nope, j = e - h * d_nope;
+        dn[e] = from_f<T>(src[(size_t)h * dq + j]);
+    }
+    for (int e = threadIdx.x; e < heads * half_r; e += blockDim.x) {
+        const int h = e / half_r, j = e - h * half_r;
+        const float x0 = src[(size_t)h * dq + d_nope + 2 * j];
+        const float x1 = src[(size_t)h * dq + d_nope + 2 * j + 1];
+        const float c = cs[2 * j], s = cs[2 * j + 1];
+        dp[(size_t)h * d_rope + 2 * j] = from_f<T>(x0 * c - x1 * s);
+        dp[(size_t)h * d_rope + 2 * j + 1] = from_f<T>(x0 * s + x1 * c);
     }
 }
 
 cudaError_t launch_q_split_rope(const float* q_all, int batch, int heads, int d_nope,
                                 int d_rope, const int32_t* pos, double rope_base, void* q_nope,
                                 void* q_pe, int dtype, cudaStream_t st) {
-    dim3 grid(batch, heads);
+    const size_t sm = (size_t)(d_rope > 0 ? d_rope : 2) * sizeof(float);
     if (dtype == MLA_DTYPE_BF16)
-        q_split_rope_kernel<__nv_bfloat16><<<grid, 64, 0, st>>>(
+        q_split_rope_kernel<__nv_bfloat16><<<batch, 256, sm, st>>>(
             q_all, heads, d_nope, d_rope, pos, rope_base, (__nv_bfloat16*)q_nope,
             (__nv_bfloat16*)q_pe);
     else
-        q_split_rope_kernel<float><<<grid, 64, 0, st>>>(q_all, heads, d_nope, d_rope, pos,
-                                                        rope_base, (float*)q_nope,
-                                                        (float*)q_pe);
+        q_split_rope_kernel<float><<<batch, 256, sm, st>>>(q_all, heads, d_nope, d_rope, pos,
+                                                          rope_base, (float*)q_nope,
+                                                          (float*)q_pe);
     return cudaGetLastError();
 }
 
