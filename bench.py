@@ -90,29 +90,35 @@ def peaks():
 
 
 def work_per_step(w):
-    """Algorithmic cache bytes and flops of one mla_decode call.
+    """Algorithmic cache bytes and flops of one decode call.
 
-    Per (query, cached token): the cache row (d_latent + d_rope elements) is
-    read once, and each head does a (d_latent + d_rope) dot product for the
-    score and a d_latent axpy for the latent-space value sum.
+    Per (query, cached token): each head does a (d_latent + d_rope) dot
+    product for the score and a d_latent axpy for the latent-space value sum.
+    Each cached row (d_latent + d_rope elements) is read from HBM once per
+    step, however many of the sequence's new tokens attend to it.  With T new
+    tokens per sequence, token j of a sequence of n sees n - T + 1 + j rows.
+    Returns (cached tokens, bytes, flops).
     """
     c = w["cfg"]
     esz = 2 if c["dtype"] == "bf16" else 4
-    tokens = int(w["seq_lens"].sum())
+    T = w.get("q_tokens", 1)
+    lens = w["seq_lens"].long()
+    rows_seen = int((lens * T - T * (T - 1) // 2).sum())
     D = c["d_latent"] + c["d_rope"]
-    bytes_ = tokens * D * esz
-    flops = tokens * c["heads"] * (2 * D + 2 * c["d_latent"])
-    return tokens, bytes_, flops
+    bytes_ = int(lens.sum()) * D * esz
+    flops = rows_seen * c["heads"] * (2 * D + 2 * c["d_latent"])
+    return int(lens.sum()), bytes_, flops
 
 
-def profile_record(kernel_tag):
-    """Per-launch DRAM traffic of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+def profile_record(kernel_tag, workload):
+    """Per-launch DRAM traffic of the decode kernel on this workload from the
+    committed ncu summary, if it was taken on the current kernel source; else
+    None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get(kernel_tag)
+        rec = json.load(f).get(f"{kernel_tag}:{workload}")
     if not rec:
         return None
     src = os.path.join(ROOT, "head_latent_attention_23_b300", "csrc", rec["source"])
@@ -221,22 +227,31 @@ def cpu_sample(w, seconds_target=12.0, max_rounds=64):
     done_heads = 0
     t0 = time.perf_counter()
     rounds = 0
+    T = w.get("q_tokens", 1)
     while True:
         pairs = [(0, (done_heads + k) % H) for k in range(threads)]
-        if w["kind"] == "cached":
-            O.reference_cached_decode(v, pairs=pairs)
-        else:
-            O.reference_token_decode(v, seqs=[0], pairs=[(0, h) for _, h in pairs])
+        _oracle_pairs(O, v, w, pairs, done_heads // H, T)
         done_heads += threads
         rounds += 1
         el = time.perf_counter() - t0
         if el >= seconds_target or rounds >= max_rounds:
             break
-    tokens = done_heads / H          # one decode token = all heads of one sequence
+    tokens = done_heads / H          # one decode token = all heads of one query token
     n0 = int(w["seq_lens"][0])
-    desc = (f"{done_heads} (sequence, head) pairs of sequence 0 (context {n0}) of "
+    desc = (f"{done_heads} (query token, head) pairs of sequence 0 (context {n0}) of "
             f"{w_name(w)}; {tokens:.3f} decode tokens in {el:.2f} s")
     return tokens / el, threads, desc
+
+
+def _oracle_pairs(O, v, w, pairs, round_idx, T):
+    """The oracle on (sequence 0, head) pairs; with several new tokens per
+    sequence, on query token round_idx % T of sequence 0."""
+    if w["kind"] == "cached":
+        O.reference_cached_decode(v, pairs=pairs)
+    elif w["kind"] == "multi":
+        O.reference_multi_decode(v, pairs=[(0, round_idx % T, h) for _, h in pairs])
+    else:
+        O.reference_token_decode(v, seqs=[0], pairs=[(0, h) for _, h in pairs])
 
 
 def w_name(w):
@@ -255,12 +270,11 @@ def run_reference(args):
     threads = O.num_threads()
     K = args.steps if args.steps else 5
 
+    T = w.get("q_tokens", 1)
+
     def step(i):
         pairs = [(0, (i * threads + k) % H) for k in range(threads)]
-        if w["kind"] == "cached":
-            O.reference_cached_decode(v, pairs=pairs)
-        else:
-            O.reference_token_decode(v, seqs=[0], pairs=[(0, h) for _, h in pairs])
+        _oracle_pairs(O, v, w, pairs, i * threads // H, T)
 
     for i in range(args.warmup):
         step(i)
@@ -287,7 +301,8 @@ def run_reference(args):
 def config_block(w, name, replicas, l2):
     c = w["cfg"]
     lens = w["seq_lens"]
-    return {"workload": name, "batch": int(w["batch"]), "heads": c["heads"],
+    return {"workload": name, "batch": int(w["batch"]), "q_tokens": int(w.get("q_tokens", 1)),
+            "heads": c["heads"],
             "d_latent": c["d_latent"], "d_rope": c["d_rope"], "d_nope": c["d_nope"],
             "d_v": c["d_v"], "block_size": c["block_size"],
             "context_min": int(lens.min()), "context_max": int(lens.max()),
@@ -317,6 +332,7 @@ def run_ours(args):
     steps = [DecodeStep(w, dev) for _ in range(R)]
     stream = torch.cuda.current_stream(dev)
     B = w["batch"]
+    units = B * w.get("q_tokens", 1)   # query tokens decoded per step
 
     for i in range(max(args.warmup, 3)):
         steps[i % R].run()
@@ -382,7 +398,7 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     # tokens of all ranks over the slowest rank's time
-    value, total_ms = job_rate(start.elapsed_time(end), B * K, dev)
+    value, total_ms = job_rate(start.elapsed_time(end), units * K, dev)
     if graph_d is not None:
         graph_d.replay()
         graph_d.replay()
@@ -394,8 +410,12 @@ def run_ours(args):
     # end to end: pinned host inputs -> device, step, result -> host
     if ws > 1:
         dist.barrier()
-    e2e = run_e2e(steps[0], w, dev, stream) if steps[0].fused else \
-        {"value": None, "unit": UNIT, "note": "workload appends several rows per sequence"}
+    if steps[0].fused:
+        e2e = run_e2e(steps[0], w, dev, stream)
+    elif steps[0].kind == "multi":
+        e2e = run_e2e_calls(steps[0], units, dev, stream)
+    else:
+        e2e = {"value": None, "unit": UNIT, "note": "workload appends several rows per sequence"}
 
     if rank != 0:
         if ws > 1:
@@ -410,7 +430,7 @@ def run_ours(args):
     t_roof = max(cbytes / (pk["hbm"] * 1e9), cflops / (pk["tc"] * 1e12))
     bound = "hbm" if cbytes / (pk["hbm"] * 1e9) >= cflops / (pk["tc"] * 1e12) else "tensor"
     path = mla.decode_path(steps[0].cfg)
-    rec = profile_record("decode_tc" if path == 1 else "decode_simt")
+    rec = profile_record("decode_tc" if path == 1 else "decode_simt", args.workload)
     roof = {
         "bound": bound,
         "achieved": hbm_gbs if bound == "hbm" else tflops,
@@ -418,7 +438,9 @@ def run_ours(args):
         "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
         "frac": (hbm_gbs / pk["hbm"]) if bound == "hbm" else (tflops / pk["tc"]),
         "traffic": rec["dram_bytes_per_launch"] if rec else None,
-        "kernel": "mla_decode (split-KV core + combine), one call per step",
+        "kernel": ("mla_decode_multi (row expansion, split-KV core + combine)"
+                   if steps[0].kind == "multi" else
+                   "mla_decode (split-KV core + combine)") + ", one call per step",
         "algorithmic_bytes_per_launch": cbytes,
         "algorithmic_flops_per_launch": cflops,
         "tensor_tflops": tflops,
@@ -484,22 +506,13 @@ def capture(step_list, ev_pairs, fused=False):
 def _run_with_decode_events(s, evpair, stream):
     """One step, with CUDA events around its mla_decode call when evpair is
     given."""
-    from head_latent_attention_23_b300 import mla
-    if s.kind == "token":
-        mla.query_proj(s.cfg, s.x_q, s.w_uq, s.pos_q, s.q_nope, s.q_pe, w_dq=s.w_dq,
-                       scratch=s.q_scratch)
-        mla.append_latent(s.cfg, s.x_new, s.w_dkv, s.seq_idx_new, s.pos_new, s.block_table,
-                          s.cache)
-    mla.absorb_q(s.cfg, s.q_nope, s.w_uk, s.q_lat)
+    s.pre()
     if evpair:
         evpair[0].record(stream)
     s.decode()
     if evpair:
         evpair[1].record(stream)
-    if s.kind == "token":
-        mla.project_out(s.cfg, s.o_lat, s.w_uv, s.o_v, s.w_o, s.out)
-    else:
-        mla.project_out(s.cfg, s.o_lat, s.w_uv, s.o_v)
+    s.post()
 
 
 def run_e2e(s, w, dev, stream, min_steps=500, min_seconds=1.0):
@@ -549,6 +562,49 @@ def run_e2e(s, w, dev, stream, min_steps=500, min_seconds=1.0):
             "call": "mla_cached_decode_step" if s.kind == "cached" else "mla_layer_decode_step",
             "note": ("one library call per step with pinned host inputs and output; "
                      "same input set every step")}
+
+
+def run_e2e_calls(s, units, dev, stream, min_steps=500, min_seconds=1.0):
+    """End to end for a step that has no single-call form (several new query
+    tokens per sequence): each step copies its inputs (queries, lengths, block
+    table) from pinned host memory to the device, issues the step's library
+    calls and copies o_v back to pinned host memory, all on one stream inside
+    the timed region."""
+    names = ["q_nope", "q_pe", "seq_lens", "block_table"]
+    dev_t = {n: getattr(s, n) for n in names}
+    host_in = {n: t.cpu().pin_memory() for n, t in dev_t.items()}
+    host_out = torch.empty(s.o_v.shape, dtype=s.o_v.dtype).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for h in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def step():
+        for n in names:
+            dev_t[n].copy_(host_in[n], non_blocking=True)
+        s.run()
+        host_out.copy_(s.o_v, non_blocking=True)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(50):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    per = a.elapsed_time(b) / 50 / 1e3
+    K = int(max(min_steps, min(min_seconds / max(per, 1e-7), 200000)))
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    value, total = job_rate(a.elapsed_time(b), units * K, dev)
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": total / K, "steps": K,
+            "call": "mla_absorb_q + mla_decode_multi + mla_project_out",
+            "note": ("pinned host inputs copied in and o_v copied out on the step's stream "
+                     "every step; same input set every step")}
 
 
 def main():

@@ -152,6 +152,30 @@ __global__ void step_positions_kernel(const int32_t* __restrict__ seq_lens, int 
     seq_idx[b] = b;
 }
 
+// Rows of a multi-token decode: query token j of sequence b (the last
+// q_tokens tokens of a sequence of n) sits at position n - q_tokens + j and
+// attends to the n - q_tokens + j + 1 tokens up to it, through the
+// sequence's own block table.  Row r = b * q_tokens + j gets that length and
+// a copy of row b of the block table.  Lengths below 1 stay as they are (the
+// decode flags and skips them).
+__global__ void expand_rows_kernel(const int32_t* __restrict__ seq_lens,
+                                   const int32_t* __restrict__ block_table, int batch,
+                                   int q_tokens, int max_blocks, int32_t* __restrict__ lens_x,
+                                   int32_t* __restrict__ table_x) {
+    const int r = blockIdx.x, b = r / q_tokens, j = r - b * q_tokens;
+    if (threadIdx.x == 0) lens_x[r] = seq_lens[b] - q_tokens + 1 + j;
+    for (int i = threadIdx.x; i < max_blocks; i += blockDim.x)
+        table_x[(size_t)r * max_blocks + i] = block_table[(size_t)b * max_blocks + i];
+}
+
+cudaError_t launch_expand_rows(const int32_t* seq_lens, const int32_t* block_table, int batch,
+                               int q_tokens, int max_blocks, int32_t* lens_x, int32_t* table_x,
+                               cudaStream_t st) {
+    expand_rows_kernel<<<batch * q_tokens, 128, 0, st>>>(seq_lens, block_table, batch, q_tokens,
+                                                         max_blocks, lens_x, table_x);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_step_positions(const int32_t* seq_lens, int batch, int32_t* pos,
                                   int32_t* seq_idx, cudaStream_t st) {
     step_positions_kernel<<<(batch + 255) / 256, 256, 0, st>>>(seq_lens, batch, pos, seq_idx);

@@ -84,6 +84,12 @@ cudaError_t launch_q_split_rope(const float* q_all, int batch, int heads, int d_
                                 int d_rope, const int32_t* pos, double rope_base, void* q_nope,
                                 void* q_pe, int dtype, cudaStream_t st);
 
+// Multi-token decode rows: lens_x[b * T + j] = seq_lens[b] - T + 1 + j and a
+// copy of block-table row b for each of them.
+cudaError_t launch_expand_rows(const int32_t* seq_lens, const int32_t* block_table, int batch,
+                               int q_tokens, int max_blocks, int32_t* lens_x, int32_t* table_x,
+                               cudaStream_t st);
+
 // pos[b] = seq_lens[b] - 1, seq_idx[b] = b (device arrays of one decode step).
 cudaError_t launch_step_positions(const int32_t* seq_lens, int batch, int32_t* pos,
                                   int32_t* seq_idx, cudaStream_t st);

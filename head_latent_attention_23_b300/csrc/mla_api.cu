@@ -303,6 +303,49 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
     return cuda_rc(launch_combine_planned(a, cfg->dtype, st));
 }
 
+int mla_decode_multi_workspace_size(const mla_config* cfg, int batch, int q_tokens,
+                                    int max_blocks, size_t* bytes) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (!bytes || batch < 1 || q_tokens < 1 || q_tokens > 64 || max_blocks < 1 ||
+        (int64_t)batch * q_tokens > kMaxDecodeBatch)
+        return MLA_ERR_INVALID_ARG;
+    const int rows = batch * q_tokens;
+    int W;
+    if (int rc = decode_workers(cfg, rows, &W)) return rc;
+    *bytes = align256((size_t)rows * 4) + align256((size_t)rows * max_blocks * 4) +
+             decode_ws_bytes(cfg, W, rows);
+    return MLA_OK;
+}
+
+int mla_decode_multi(const mla_config* cfg, const void* q_lat, const void* q_pe,
+                     const void* cache, int64_t num_blocks, const int32_t* block_table,
+                     int max_blocks, const int32_t* seq_lens, int batch, int q_tokens,
+                     void* o_lat, float* lse, void* workspace, size_t ws_bytes,
+                     mla_stream_t stream) {
+    if (int rc = check_cfg(cfg)) return rc;
+    if (batch < 1 || q_tokens < 1 || q_tokens > 64 || max_blocks < 1 || num_blocks < 1 ||
+        (int64_t)batch * q_tokens > kMaxDecodeBatch)
+        return MLA_ERR_INVALID_ARG;
+    if (!q_lat || (!q_pe && cfg->d_rope > 0) || !cache || !block_table || !seq_lens || !o_lat)
+        return MLA_ERR_INVALID_ARG;
+    size_t need;
+    if (int rc = mla_decode_multi_workspace_size(cfg, batch, q_tokens, max_blocks, &need))
+        return rc;
+    if (!workspace || ws_bytes < need || ((uintptr_t)workspace & 255)) return MLA_ERR_WORKSPACE;
+    const int rows = batch * q_tokens;
+    char* p = (char*)workspace;
+    int32_t* lens_x = (int32_t*)p;
+    p += align256((size_t)rows * 4);
+    int32_t* table_x = (int32_t*)p;
+    p += align256((size_t)rows * max_blocks * 4);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (launch_expand_rows(seq_lens, block_table, batch, q_tokens, max_blocks, lens_x, table_x,
+                           st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    return mla_decode(cfg, q_lat, q_pe, cache, num_blocks, table_x, max_blocks, lens_x, rows,
+                      o_lat, lse, p, ws_bytes - (size_t)(p - (char*)workspace), stream);
+}
+
 int mla_decode_combine(const mla_config* cfg, const float* o_part, const float* lse_part,
                        int n_splits, int batch, void* o_lat, float* lse, mla_stream_t stream) {
     if (int rc = check_cfg(cfg)) return rc;

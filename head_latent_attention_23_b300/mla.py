@@ -33,6 +33,7 @@ EXPORTS = (
     "mla_decode_combine", "mla_project_out", "mla_query_proj_workspace_size", "mla_query_proj",
     "mla_decode_noalloc", "mla_set_wait_limit_ns", "mla_layer_decode_step_workspace_size",
     "mla_layer_decode_step", "mla_cached_decode_step_workspace_size", "mla_cached_decode_step",
+    "mla_decode_multi_workspace_size", "mla_decode_multi",
 )
 
 IO_HOST_INPUTS = 1
@@ -112,6 +113,9 @@ def lib():
         L.mla_layer_decode_step.argtypes = [CP, LW, P, P, I, P, I64, P, I, P, I, P,
                                             ctypes.c_size_t, P]
         L.mla_cached_decode_step_workspace_size.argtypes = [CP, I, I, SZ]
+        L.mla_decode_multi_workspace_size.argtypes = [CP, I, I, I, SZ]
+        L.mla_decode_multi.argtypes = [CP, P, P, P, I64, P, I, P, I, I, P, P, P, ctypes.c_size_t,
+                                       P]
         L.mla_cached_decode_step.argtypes = [CP, P, P, P, P, P, I, P, I64, P, I, P, P, P, I, P,
                                              ctypes.c_size_t, P]
         for name in EXPORTS:
@@ -350,3 +354,31 @@ def cached_decode_step(cfg, q_nope, q_pe, w_uk, w_uv, seq_lens, cache, block_tab
         int(io_flags), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "mla_cached_decode_step")
+
+
+def decode_multi_workspace_size(cfg, batch, q_tokens, max_blocks):
+    n = ctypes.c_size_t(0)
+    _check(lib().mla_decode_multi_workspace_size(ctypes.byref(cfg), batch, q_tokens, max_blocks,
+                                                  ctypes.byref(n)),
+           "mla_decode_multi_workspace_size")
+    return n.value
+
+
+def decode_multi(cfg, q_lat, q_pe, cache, block_table, seq_lens, o_lat, lse=None,
+                 workspace=None, stream=None):
+    """mla_decode_multi: q_lat [batch][q_tokens][heads][d_latent], the last
+    q_tokens tokens of each sequence with the causal mask among them."""
+    dt = _tdtype(cfg)
+    batch, max_blocks = block_table.shape
+    q_tokens = q_lat.shape[1]
+    if workspace is None:
+        workspace = torch.empty(decode_multi_workspace_size(cfg, batch, q_tokens, max_blocks),
+                                dtype=torch.uint8, device=q_lat.device)
+    rc = lib().mla_decode_multi(
+        ctypes.byref(cfg), _ptr(q_lat, dt, "q_lat"), _ptr(q_pe, dt, "q_pe"),
+        _ptr(cache, dt, "cache"), cache.shape[0], _ptr(block_table, torch.int32, "block_table"),
+        max_blocks, _ptr(seq_lens, torch.int32, "seq_lens"), batch, q_tokens,
+        _ptr(o_lat, dt, "o_lat"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(rc, "mla_decode_multi")

@@ -6,6 +6,8 @@ one stream.  Nothing here computes: it only orders the calls.
 
 Step for a workload whose cache rows are given (shared-cache decode):
     mla_absorb_q -> mla_decode (split-KV core + combine) -> mla_project_out
+Step for several new query tokens per sequence over such a cache:
+    mla_absorb_q (all tokens) -> mla_decode_multi -> mla_project_out
 Step for a workload driven by hidden states x (full layer):
     mla_query_proj -> mla_append_latent -> mla_absorb_q -> mla_decode
     -> mla_project_out (with W_O)
@@ -42,7 +44,9 @@ class DecodeStep:
         self.w_uk = up("w_uk")
         self.w_uv = up("w_uv")
         self.B = B
-        if self.kind == "cached":
+        self.T = w.get("q_tokens", 1)
+        rows = B * self.T             # query rows: one per (sequence, new token)
+        if self.kind in ("cached", "multi"):
             self.q_nope = up("q_nope")
             self.q_pe = up("q_pe")
         else:
@@ -61,17 +65,22 @@ class DecodeStep:
             self.q_scratch = torch.empty(mla.query_proj_workspace_size(self.cfg, B, d_lq),
                                          dtype=torch.uint8, device=dev)
             self.out = torch.empty((B, w["d_model"]), dtype=dt, device=dev)
-        self.q_lat = torch.empty((B, H, c["d_latent"]), dtype=dt, device=dev)
-        self.o_lat = torch.empty((B, H, c["d_latent"]), dtype=dt, device=dev)
-        self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
-        self.o_v = torch.empty((B, H, c["d_v"]), dtype=dt, device=dev)
-        self.workspace = mla.decode_workspace(self.cfg, B, dev)
+        self.q_lat = torch.empty((rows, H, c["d_latent"]), dtype=dt, device=dev)
+        self.o_lat = torch.empty((rows, H, c["d_latent"]), dtype=dt, device=dev)
+        self.lse = torch.empty((rows, H), dtype=torch.float32, device=dev)
+        self.o_v = torch.empty((rows, H, c["d_v"]), dtype=dt, device=dev)
         maxb = self.block_table.shape[1]
+        if self.kind == "multi":
+            self.workspace = torch.empty(
+                mla.decode_multi_workspace_size(self.cfg, B, self.T, maxb), dtype=torch.uint8,
+                device=dev)
+        else:
+            self.workspace = mla.decode_workspace(self.cfg, B, dev)
         # one library call per step: the shared-cache step, or the full layer
         # step when each sequence gets exactly one new token (its newest)
         self.fused = self.kind == "cached" or (
-            w["x_new"].shape[0] == B and torch.equal(w["x_new"], w["x_q"]) and
-            torch.equal(w["seq_idx_new"], torch.arange(B, dtype=torch.int32)) and
+            self.kind == "token" and w["x_new"].shape[0] == B and
+            torch.equal(w["x_new"], w["x_q"]) and torch.equal(w["seq_idx_new"], torch.arange(B, dtype=torch.int32)) and
             torch.equal(w["pos_new"], w["seq_lens"] - 1))
         if self.kind == "cached":
             n = mla.cached_decode_step_workspace_size(self.cfg, B, maxb)
@@ -85,22 +94,37 @@ class DecodeStep:
 
     # the graded core: split-KV attention + combine
     def decode(self, stream=None):
-        mla.decode(self.cfg, self.q_lat, self.q_pe, self.cache, self.block_table,
-                   self.seq_lens, self.o_lat, self.lse, self.workspace, stream)
+        if self.kind == "multi":
+            B, T, H = self.B, self.T, self.cfg_dict["heads"]
+            mla.decode_multi(self.cfg, self.q_lat.view(B, T, H, -1), self.q_pe, self.cache,
+                             self.block_table, self.seq_lens, self.o_lat.view(B, T, H, -1),
+                             self.lse.view(B, T, H), self.workspace, stream)
+        else:
+            mla.decode(self.cfg, self.q_lat, self.q_pe, self.cache, self.block_table,
+                       self.seq_lens, self.o_lat, self.lse, self.workspace, stream)
 
-    def run(self, stream=None):
+    def pre(self, stream=None):
+        """The step's calls before mla_decode."""
         if self.kind == "token":
             mla.query_proj(self.cfg, self.x_q, self.w_uq, self.pos_q, self.q_nope, self.q_pe,
                            w_dq=self.w_dq, scratch=self.q_scratch, stream=stream)
             mla.append_latent(self.cfg, self.x_new, self.w_dkv, self.seq_idx_new, self.pos_new,
                               self.block_table, self.cache, stream=stream)
-        mla.absorb_q(self.cfg, self.q_nope, self.w_uk, self.q_lat, stream)
-        self.decode(stream)
+        q_nope = self.q_nope.reshape(self.q_lat.shape[0], self.q_lat.shape[1], -1)
+        mla.absorb_q(self.cfg, q_nope, self.w_uk, self.q_lat, stream)
+
+    def post(self, stream=None):
+        """The step's calls after mla_decode."""
         if self.kind == "token":
             mla.project_out(self.cfg, self.o_lat, self.w_uv, self.o_v, self.w_o, self.out,
                             stream)
         else:
             mla.project_out(self.cfg, self.o_lat, self.w_uv, self.o_v, stream=stream)
+
+    def run(self, stream=None):
+        self.pre(stream)
+        self.decode(stream)
+        self.post(stream)
 
     def run_fused(self, io_flags=0, inputs=None, result=None, stream=None):
         """The step as one library call.  With io_flags, `inputs` (dict of
@@ -130,6 +154,8 @@ class DecodeStep:
         The fused full-layer step adds the positions kernel and a split-K
         reduction after each batch-1 projection that splits K."""
         n = 1 + 2 + 1                       # absorb, decode core + combine, o_v
+        if self.kind == "multi":
+            n += 1                          # per-token rows of the split plan
         if self.kind == "token":
             n += (2 if self.w_dq is not None else 1) + 1   # query GEMM(s) + split/rope
             n += 1                          # append
@@ -165,6 +191,8 @@ class DecodeStep:
 
     def results(self):
         r = dict(o_lat=self.o_lat, lse=self.lse, o_v=self.o_v, q_lat=self.q_lat)
+        if self.kind == "multi":
+            r = {k: v.view(self.B, self.T, *v.shape[1:]) for k, v in r.items()}
         if self.kind == "token":
             r["out"] = self.out
             r["q_nope"] = self.q_nope

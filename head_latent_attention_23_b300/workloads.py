@@ -151,6 +151,27 @@ def crossing_ranges_decode(seed=31, batch=80, d_nope=64, d_v=8):
     return cached_decode(batch, lens, seed=seed, permute=True, d_nope=d_nope, d_v=d_v)
 
 
+def multi_token_decode(batch, seq_lens, q_tokens, seed=0, permute=True):
+    """Decode of the last q_tokens tokens of each sequence at once (a chunk of
+    prefill or a speculative step), over a cache whose rows are drawn: the
+    cached_decode draws, then per-token queries q_nope [B,T,H,d_n] and q_pe
+    [B,T,H,d_r] (unit normal) replacing the single-token ones."""
+    w = cached_decode(batch, seq_lens, seed=seed, permute=permute)
+    g = torch.Generator().manual_seed(seed + 7919)
+    c = w["cfg"]
+    w["q_nope"] = _randn(g, (batch, q_tokens, c["heads"], c["d_nope"]), 1.0, c["dtype"])
+    w["q_pe"] = _randn(g, (batch, q_tokens, c["heads"], c["d_rope"]), 1.0, c["dtype"])
+    w["kind"] = "multi"
+    w["q_tokens"] = q_tokens
+    return w
+
+
+def v2_b16_ctx4k_q4(seed=0):
+    """DeepSeek-V2 attention shapes, 16 sequences of 4096 tokens, the last 4
+    tokens of each decoded at once (a 4-token speculative step)."""
+    return multi_token_decode(16, [4096] * 16, 4, seed=seed)
+
+
 def token_decode(batch, ctx, seed=0, dtype="bf16", block_size=64, permute=False,
                  heads=128, d_latent=512, d_rope=64, d_nope=128, d_v=128, d_model=7168,
                  d_lq=1536, prior_rows="random"):
@@ -239,6 +260,7 @@ def v2_layer_b128_ctx2k(seed=0):
 WORKLOADS = {
     "tiny_f32": tiny_f32,
     "v2_b16_ctx4k": v2_b16_ctx4k,
+    "v2_b16_ctx4k_q4": v2_b16_ctx4k_q4,
     "v2_ragged_b64": v2_ragged_b64,
     "v2_long_b4_ctx100k": v2_long_b4_ctx100k,
     "v2_layer_b128_ctx2k": v2_layer_b128_ctx2k,
@@ -286,7 +308,7 @@ def oracle_view(w):
     out = dict(cfg=cfg, scale=cfg["softmax_scale"], round=round_to(cfg["dtype"]),
                store=store_as(cfg["dtype"]))
     for k, v in w.items():
-        if k in ("cfg", "kind", "batch", "d_model", "d_lq"):
+        if k in ("cfg", "kind", "batch", "d_model", "d_lq", "q_tokens"):
             continue
         if k == "cache" and v.dtype == torch.bfloat16:
             out[k] = v.view(torch.int16).numpy().view(np.uint16)

@@ -189,6 +189,33 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
                size_t ws_bytes, mla_stream_t stream);
 
 /*
+ * Decode of several new query tokens per sequence at once (a chunk of
+ * prefill, or the tokens a speculative step proposes): the last q_tokens
+ * tokens of each sequence, token j at position seq_lens[b] - q_tokens + j,
+ * each attending to the cached rows up to and including its own position
+ * (the causal mask of section 03 of "How DeepSeek Rewrote the Transformer
+ * (MLA)"; section 04: with one token this is mla_decode).  The rows of the
+ * new tokens must already be in the cache.
+ *   q_lat   [batch][q_tokens][heads][d_latent]   absorbed queries
+ *   q_pe    [batch][q_tokens][heads][d_rope]     rotary parts, rotated at each token's position
+ *   seq_lens [batch] int32, tokens including the q_tokens new ones, >= q_tokens
+ *   o_lat   [batch][q_tokens][heads][d_latent]   (written)
+ *   lse     [batch][q_tokens][heads] float32 or NULL
+ *   workspace >= mla_decode_multi_workspace_size() bytes, 256-byte aligned
+ *   1 <= q_tokens <= 64, batch * q_tokens <= 8192.
+ * Each token is decoded as its own row of the split-KV plan, with the
+ * sequence's block table; the rows of one sequence are adjacent in the plan,
+ * so its cache rows are read from HBM about once and from L2 by the others.
+ */
+int mla_decode_multi_workspace_size(const mla_config* cfg, int batch, int q_tokens,
+                                    int max_blocks, size_t* bytes);
+int mla_decode_multi(const mla_config* cfg, const void* q_lat, const void* q_pe,
+                     const void* cache, int64_t num_blocks, const int32_t* block_table,
+                     int max_blocks, const int32_t* seq_lens, int batch, int q_tokens,
+                     void* o_lat, float* lse, void* workspace, size_t ws_bytes,
+                     mla_stream_t stream);
+
+/*
  * Merges partial decode results computed over disjoint token ranges of the
  * same sequences (e.g. ranges held by different devices):
  *   LSE = log sum_s exp(lse_s),  o = sum_s exp(lse_s - LSE) o_s.

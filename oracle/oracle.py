@@ -201,6 +201,30 @@ def decode(cache, block_table, seq_lens, q_nope, q_pe, w_uk, w_uv, scale, w_o=No
     return res
 
 
+def decode_multi(cache, block_table, seq_lens, q_nope, q_pe, w_uk, w_uv, scale, pairs=None):
+    """Decode of the last T tokens of each sequence at once.
+
+    q_nope [B,T,H,d_n], q_pe [B,T,H,d_r]; the cache already holds the rows of
+    the T new tokens.  Token j of sequence b sits at position n_b - T + j and
+    attends to positions 0..n_b - T + j: the causal mask of "How DeepSeek
+    Rewrote the Transformer (MLA)", section 03 ("each position attends only to
+    itself and earlier ones").  Each token is therefore one unmerged decode
+    over the n_b - T + 1 + j tokens before and at it, through its sequence's
+    block table.  pairs: iterable of (b, j, h) or None for all.  Returns o_lat
+    [B,T,H,d_l], o_v [B,T,H,d_v], lse [B,T,H].
+    """
+    q_nope = np.asarray(q_nope)
+    q_pe = np.asarray(q_pe)
+    B, T, H = q_nope.shape[:3]
+    bt = np.repeat(_i32(block_table), T, axis=0)
+    lens = np.repeat(_i32(seq_lens), T) - T + 1 + np.tile(np.arange(T, dtype=np.int32), B)
+    rp = None if pairs is None else [(b * T + j, h) for (b, j, h) in pairs]
+    r = decode(cache, bt, lens, q_nope.reshape(B * T, H, -1), q_pe.reshape(B * T, H, -1),
+               w_uk, w_uv, scale, pairs=rp)
+    return {"o_lat": r["o_lat"].reshape(B, T, H, -1), "o_v": r["o_v"].reshape(B, T, H, -1),
+            "lse": r["lse"].reshape(B, T, H)}
+
+
 def kv_numbers_per_token(kv_heads, head_dim, layers):
     return float(_L().mla_oracle_kv_numbers_per_token(kv_heads, head_dim, layers))
 
@@ -229,6 +253,13 @@ def reference_cached_decode(w, pairs=None, plant=PLANT_NONE):
     """
     return decode(w["cache"], w["block_table"], w["seq_lens"], w["q_nope"], w["q_pe"],
                   w["w_uk"], w["w_uv"], w["scale"], pairs=pairs, plant=plant)
+
+
+def reference_multi_decode(w, pairs=None):
+    """Multi-token decode over a cache whose rows are given: q_nope and q_pe
+    carry a token axis, [B,T,H,*]."""
+    return decode_multi(w["cache"], w["block_table"], w["seq_lens"], w["q_nope"], w["q_pe"],
+                        w["w_uk"], w["w_uv"], w["scale"], pairs=pairs)
 
 
 def reference_token_decode(w, pairs=None, seqs=None, plant=PLANT_NONE):

@@ -98,3 +98,17 @@ def test_step_calls_validate_on_the_host(L):
                                     None, None, 4, None, 0, None) == mla.MLA_ERR_INVALID_ARG
     assert L.mla_cached_decode_step(cp, None, None, None, None, None, 4, None, 1, None, 8, None,
                                     None, None, 0, None, 0, None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_multi_token_decode_validates_on_the_host(L):
+    c = mla.config(128, 512, 64, 128, 128, 64, "bf16")
+    cp = ctypes.byref(c)
+    n = ctypes.c_size_t(0)
+    for batch, q_tokens in ((4, 0), (4, 65), (0, 2), (200, 64)):
+        assert L.mla_decode_multi_workspace_size(cp, batch, q_tokens, 8, ctypes.byref(n)) == \
+            mla.MLA_ERR_INVALID_ARG
+        assert L.mla_decode_multi(cp, None, None, None, 1, None, 8, None, batch, q_tokens, None,
+                                  None, None, 0, None) == mla.MLA_ERR_INVALID_ARG
+    # a valid shape with null tensors is refused before any CUDA call
+    assert L.mla_decode_multi(cp, None, None, None, 1, None, 8, None, 4, 2, None, None, None, 0,
+                              None) == mla.MLA_ERR_INVALID_ARG

@@ -36,6 +36,16 @@ def test_work_per_token_matches_the_pages_cache_row():
     assert flops == heads * 2 * ((dl + dr) + dl) == 278_528
 
 
+def test_work_of_several_new_tokens_reads_each_row_once():
+    """Four new tokens per sequence: the cache bytes stay one row per cached
+    token, the flops count token j of a sequence of n over n - 3 + j rows."""
+    w = {"cfg": _cfg(), "seq_lens": torch.tensor([4, 10]), "q_tokens": 4}
+    tokens, nbytes, flops = bench.work_per_step(w)
+    assert tokens == 14
+    assert nbytes == 14 * 576 * 2
+    assert flops == (1 + 2 + 3 + 4 + 7 + 8 + 9 + 10) * 128 * 2 * (576 + 512)
+
+
 def test_work_of_the_batch16_4k_call():
     w = {"cfg": _cfg(), "seq_lens": torch.tensor([4096] * 16)}
     tokens, nbytes, flops = bench.work_per_step(w)
@@ -66,24 +76,25 @@ def _write_profile(root, sha):
     (csrc / "decode_tc.cu").write_bytes(b"// kernel source\n")
     (root / "profiles").mkdir()
     (root / "profiles" / "ncu_traffic.json").write_text(json.dumps(
-        {"decode_tc": {"source": "decode_tc.cu", "source_sha": sha,
+        {"decode_tc:v2_b16_ctx4k": {"source": "decode_tc.cu", "source_sha": sha,
                        "dram_bytes_per_launch": 123}}))
 
 
 def test_traffic_is_used_only_for_the_profiled_source(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.profile_record("decode_tc") is None          # no record at all
+    assert bench.profile_record("decode_tc", "v2_b16_ctx4k") is None    # no record at all
     sha = hashlib.sha256(b"// kernel source\n").hexdigest()[:16]
     _write_profile(tmp_path, sha)
-    assert bench.profile_record("decode_tc")["dram_bytes_per_launch"] == 123
-    assert bench.profile_record("decode_simt") is None         # no record for that kernel
+    assert bench.profile_record("decode_tc", "v2_b16_ctx4k")["dram_bytes_per_launch"] == 123
+    assert bench.profile_record("decode_simt", "v2_b16_ctx4k") is None   # not that kernel
+    assert bench.profile_record("decode_tc", "v2_b16_ctx4k_q4") is None  # not that workload
     (tmp_path / "head_latent_attention_23_b300" / "csrc" / "decode_tc.cu").write_bytes(
         b"// kernel source, changed\n")
-    assert bench.profile_record("decode_tc") is None          # kernel changed since
+    assert bench.profile_record("decode_tc", "v2_b16_ctx4k") is None    # kernel changed since
 
 
 def test_committed_traffic_record_is_plausible():
-    rec = bench.profile_record("decode_tc")
+    rec = bench.profile_record("decode_tc", "v2_b16_ctx4k")
     if rec is None:
         # the kernel changed since its capture: bench.py reports traffic null
         pytest.skip("profiles/ncu_traffic.json predates the current decode_tc.cu")

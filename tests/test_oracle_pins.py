@@ -207,6 +207,30 @@ def test_decode_step_is_last_row_of_causal_prefill():
         assert _rel(res["o_v"][0], o_full[0, :, t, :]) < 1e-12
 
 
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_multi_token_decode_is_last_rows_of_causal_prefill(T):
+    """Several new tokens decoded at once are the last T rows of full causal
+    attention (torch SDPA with its causal mask over explicitly multiplied-out
+    keys), sequences of different lengths in one batch."""
+    p = _small_token_problem(6, d_r=4, B=2)
+    n = p["n"]
+    _, o_full = _mha_reference(p, causal_rows=True)     # [B, H, n, d_v]
+    lens = np.array([n, n - 1], dtype=np.int32)
+    qn, qp = [], []
+    for b in range(p["B"]):
+        pos = np.arange(lens[b] - T, lens[b], dtype=np.int32)
+        a, c = O.query(p["x"][b, pos, :], p["w_uq"], p["H"], p["d_n"], p["d_r"], pos,
+                       w_dq=p["w_dq"])
+        qn.append(a)
+        qp.append(c)
+    res = O.decode_multi(p["cache"], p["bt"], lens, np.stack(qn), np.stack(qp), p["w_uk"],
+                         p["w_uv"], p["scale"])
+    for b in range(p["B"]):
+        for j in range(T):
+            t = lens[b] - T + j
+            assert _rel(res["o_v"][b, j], o_full[b, :, t, :]) < 1e-12
+
+
 def test_merged_weights_give_the_same_scores_and_output():
     """The two merges of "Two merges are where the compute win comes from":
     W_LQK_h = W_LQQ_h W_LK_h^T acting on latents, and W_LO_h = W_LV_h W_O_h,

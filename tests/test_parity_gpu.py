@@ -203,6 +203,68 @@ def test_split_ranges_crossing_sequences_all_pairs():
     assert rel(host(lse), ref["lse"]) <= TOL["bf16"]
 
 
+# ---------------------------------------------------------------- several new tokens
+
+@pytest.mark.parametrize("T,lens", [(2, [2, 3, 64, 65, 129, 700]),
+                                    (4, [4, 5, 127, 128, 131, 1000, 3000])])
+def test_multi_token_decode_all_pairs(T, lens):
+    """The last T tokens of each sequence decoded at once, token j seeing the
+    n - T + 1 + j tokens up to it (causal mask, "How DeepSeek Rewrote the
+    Transformer (MLA)", section 03).  Lengths put the first new token on one
+    row (n = T) and the masked edge on both sides of the 64-token page and
+    128-token tile boundaries; pages permuted.  Every (sequence, token, head)
+    triple of o_lat, o_v and lse."""
+    w = W.multi_token_decode(len(lens), lens, T, seed=40 + T)
+    step = run_step(w)
+    ref = O.reference_multi_decode(W.oracle_view(w))
+    res = step.results()
+    for key in ("o_lat", "o_v", "lse"):
+        assert rel(host(res[key]), ref[key]) <= TOL["bf16"], key
+
+
+def test_multi_token_decode_mask_and_single_token_equivalence():
+    """Raising the newest cached row of each sequence changes the outputs of
+    its last new token only; the other tokens stay bit-identical.  With one
+    new token the call equals mla_decode bit for bit."""
+    T, lens = 3, [3, 90, 200]
+    w = W.multi_token_decode(len(lens), lens, T, seed=52)
+    a = run_step(w)
+    o1 = host(a.results()["o_lat"]).copy()
+    bt = w["block_table"].numpy()
+    for b, n in enumerate(lens):
+        w["cache"][bt[b, (n - 1) // 64], (n - 1) % 64, :] *= 3.0
+    o2 = host(run_step(w).results()["o_lat"])
+    assert np.array_equal(o1[:, :T - 1], o2[:, :T - 1])
+    for b in range(len(lens)):
+        assert not np.array_equal(o1[b, T - 1], o2[b, T - 1])
+
+    w1 = W.multi_token_decode(len(lens), lens, 1, seed=53)
+    m = run_step(w1)
+    cfg = mla.config_from(w1["cfg"])
+    o_lat = torch.empty_like(m.o_lat)
+    lse = torch.empty_like(m.lse)
+    mla.decode(cfg, m.q_lat, m.q_pe.view(len(lens), 128, -1), m.cache, m.block_table,
+               m.seq_lens, o_lat, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(o_lat, m.o_lat) and torch.equal(lse, m.lse)
+
+
+def test_multi_token_full_size_sampled():
+    """16 sequences of 4096 tokens, the last 4 of each decoded at once: all
+    tokens and heads of sequences 0, 7 and 15."""
+    w = W.v2_b16_ctx4k_q4()
+    step = run_step(w)
+    pairs = [(b, j, h) for b in (0, 7, 15) for j in range(4) for h in range(128)]
+    ref = O.reference_multi_decode(W.oracle_view(w), pairs=pairs)
+    res = step.results()
+    bi = np.array([p[0] for p in pairs])
+    ji = np.array([p[1] for p in pairs])
+    hi = np.array([p[2] for p in pairs])
+    for key in ("o_lat", "o_v", "lse"):
+        assert rel(host(res[key])[bi, ji, hi], np.asarray(ref[key])[bi, ji, hi]) <= \
+            TOL["bf16"], key
+
+
 def _host_pinned(t):
     return t.cpu().pin_memory()
 
