@@ -364,13 +364,15 @@ def run_ours(args):
     rem = K - (K // G) * G
     dec_ev = [(torch.cuda.Event(enable_timing=True, external=True),
                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(G)]
-    # A full-layer step is timed as the one library call a user makes
-    # (mla_layer_decode_step, whose batch-1 projections split K over all SMs);
-    # its mla_decode durations come from a replay of the same step issued as
-    # separate calls with events around mla_decode, right after the timed
-    # region.  Shared-cache steps issue the same kernels either way and are
-    # timed as separate calls with the events inside.
-    fused_timing = steps[0].kind == "token" and steps[0].fused
+    # A step is timed as the one library call a user makes
+    # (mla_cached_decode_step, or mla_layer_decode_step, whose batch-1
+    # projections split K over all SMs), its kernels chained by programmatic
+    # dependent launch; the mla_decode durations come from a replay of the
+    # same steps issued as separate calls with events around mla_decode,
+    # right after the timed region (an event between two kernels ends their
+    # overlap, so the events stay out of the timed replays).  Steps with no
+    # single-call form are timed as separate calls with the events inside.
+    fused_timing = steps[0].fused
     if fused_timing:
         graph_a = capture(ga_steps, None, fused=True)
         graph_b = capture([steps[i % R] for i in range(rem)], None, fused=True) if rem else None
@@ -473,8 +475,9 @@ def run_ours(args):
         "gpu_launches": K * steps[0].kernels_per_step(fused=fused_timing),
         "timing": (f"CUDA graphs of {G} steps replayed {K // G} times"
                    + (f" + one of {rem} steps" if rem else "")
-                   + ("; each step one mla_layer_decode_step call; mla_decode durations from "
-                      "events in a replay of the step as separate calls" if fused_timing else
+                   + (f"; each step one {'mla_cached_decode_step' if steps[0].kind == 'cached' else 'mla_layer_decode_step'}"
+                      " call; mla_decode durations from events in a replay of the step as "
+                      "separate calls" if fused_timing else
                       "; mla_decode durations from events inside the last replay")),
         "clocks": clk.summary(),
     }

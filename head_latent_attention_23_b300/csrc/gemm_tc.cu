@@ -19,6 +19,14 @@
 // (tile, K range) pair; its epilogue writes an fp32 partial tile to
 // p.partial[split][m][n], and splitk_reduce_kernel adds the partials and
 // applies the product's epilogue (store, or RoPE and the paged scatter).
+//
+// Skinny products (p.swap).  The per-head query absorption and value
+// projection at decode batch sizes have M = batch rows: as the MMA's M side
+// they would fill 16 of its 128 rows and leave 7/8 of every epilogue idle.
+// They run transposed instead, C^T = W^T X^T: a tile is 128 output columns
+// (128 weight rows as the A operand, TMEM lanes) by the M activation rows
+// padded to np (the B operand, N = np of the MMA), so the weight stream is
+// the only large operand and each epilogue thread writes one output column.
 #include "kernels.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -27,9 +35,19 @@ namespace mla {
 
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64, kStages = 4;
+constexpr int kBM = 128, kBN = 128, kBK = 64;
 constexpr int kTileBytes = 16384;   // one 128 x 64 bf16 slice of A or of B
-constexpr int kSmemBytes = 1024 + kStages * 2 * kTileBytes + 256;
+// Ring: four stages of A and B slices; a skinny product's stage is a weight
+// slice and at most 64 activation rows (8 KB), so seven stages fit (next to
+// two CTAs of the merge kernel, which it may overlap) and most of a CTA's
+// share of the weights is in flight at once.
+template <bool kSwap>
+struct Ring {
+    static constexpr int stages = kSwap ? 7 : 4;
+    static constexpr int b_bytes = kSwap ? 8192 : kTileBytes;
+    static constexpr int smem = 1024 + stages * (kTileBytes + b_bytes) + 256;
+};
+constexpr int kSkinnyMaxRows = Ring<true>::b_bytes / 128;   // 64
 constexpr int kAcc = 2;             // TMEM accumulators: the epilogue drains one tile
                                     // while the MMAs fill the other
 
@@ -60,14 +78,16 @@ __device__ __forceinline__ void item_range(int item, int splits, int nk, int* ti
     *kt1 = (int)((int64_t)(sp + 1) * nk / splits);
 }
 
+template <bool kSwap>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                    const TcGemmParams p, int tiles_n, int tiles_m, int num_items) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
+    constexpr int kStages = Ring<kSwap>::stages, kBBytes = Ring<kSwap>::b_bytes;
     uint8_t* sB = smem + kStages * kTileBytes;
-    uint64_t* full = (uint64_t*)(sB + kStages * kTileBytes);
+    uint64_t* full = (uint64_t*)(sB + kStages * kBBytes);
     uint64_t* empty = full + kStages;
     uint64_t* acc_full = empty + kStages;
     uint64_t* acc_empty = acc_full + kAcc;
@@ -77,6 +97,7 @@ __global__ void __launch_bounds__(192, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = (p.K + kBK - 1) / kBK;
+    int pre = 0;    // skinny: slices whose weight copies went out before the wait
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -92,13 +113,32 @@ __global__ void __launch_bounds__(192, 1)
         fence_mbar_init();
         prefetch_tmap(&tA);
         prefetch_tmap(&tB);
+        if (kSwap) {
+            // No kernel this one may overlap writes the weights, so the first
+            // stages' weight slices are requested before the previous kernel
+            // has finished: their first-touch latency hides behind its tail.
+            for (int t = blockIdx.x; t < num_items && pre < kStages; t += gridDim.x) {
+                const TileId ti = tile_of(t, tiles_n, tiles_m);
+                for (int kt = 0; kt < nk && pre < kStages; ++kt, ++pre) {
+                    uint8_t* dst = sA + pre * kTileBytes;
+                    mbar_arrive_expect_tx(&full[pre], kTileBytes + p.np * 128);
+                    if (p.a_mn) {
+                        tma_load_3d(dst, &tA, ti.n0, kt * kBK, ti.z, &full[pre]);
+                        tma_load_3d(dst + kTileBytes / 2, &tA, ti.n0 + 64, kt * kBK, ti.z,
+                                    &full[pre]);
+                    } else {
+                        tma_load_3d(dst, &tA, kt * kBK, ti.n0, ti.z, &full[pre]);
+                    }
+                }
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tslot, kAcc * kBN);
         tmem_relinquish();
     }
-    // set-up above overlaps the previous kernel's tail; operands are read
-    // only once it has finished
+    // set-up above overlaps the previous kernel's tail; the activations are
+    // read, and C written, only once it has finished
     pdl_wait_primary();
     tc_fence_before();
     __syncthreads();
@@ -115,19 +155,37 @@ __global__ void __launch_bounds__(192, 1)
                 const TileId ti = tile_of(tile, tiles_n, tiles_m);
                 for (int kt = kt0; kt < kt1; ++kt, ++it) {
                     const int s = it % kStages;
+                    if (kSwap && it < pre) {
+                        // weights requested before the wait: the activations now
+                        tma_load_3d(sB + s * kBBytes, &tB, kt * kBK, 0, ti.z, &full[s]);
+                        continue;
+                    }
                     if (!mbar_wait_fast(&empty[s], ((it / kStages) & 1) ^ 1, abort_flag,
                                         p.status)) {
                         ok = false;
                         break;
                     }
+                    if (kSwap) {
+                        // weights: 128 output columns x 64 k; activations: np rows x 64 k
+                        mbar_arrive_expect_tx(&full[s], kTileBytes + p.np * 128);
+                        if (p.a_mn) {
+                            tma_load_3d(sA + s * kTileBytes, &tA, ti.n0, kt * kBK, ti.z, &full[s]);
+                            tma_load_3d(sA + s * kTileBytes + kTileBytes / 2, &tA, ti.n0 + 64,
+                                        kt * kBK, ti.z, &full[s]);
+                        } else {
+                            tma_load_3d(sA + s * kTileBytes, &tA, kt * kBK, ti.n0, ti.z, &full[s]);
+                        }
+                        tma_load_3d(sB + s * kBBytes, &tB, kt * kBK, 0, ti.z, &full[s]);
+                        continue;
+                    }
                     mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
                     tma_load_3d(sA + s * kTileBytes, &tA, kt * kBK, ti.m0, ti.z, &full[s]);
                     if (p.b_mn) {
-                        tma_load_3d(sB + s * kTileBytes, &tB, ti.n0, kt * kBK, ti.z, &full[s]);
-                        tma_load_3d(sB + s * kTileBytes + kTileBytes / 2, &tB, ti.n0 + 64,
+                        tma_load_3d(sB + s * kBBytes, &tB, ti.n0, kt * kBK, ti.z, &full[s]);
+                        tma_load_3d(sB + s * kBBytes + kTileBytes / 2, &tB, ti.n0 + 64,
                                     kt * kBK, ti.z, &full[s]);
                     } else {
-                        tma_load_3d(sB + s * kTileBytes, &tB, kt * kBK, ti.n0, ti.z, &full[s]);
+                        tma_load_3d(sB + s * kBBytes, &tB, kt * kBK, ti.n0, ti.z, &full[s]);
                     }
                 }
             }
@@ -137,12 +195,16 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(kBM, kBN, false, p.b_mn != 0);
+            const uint32_t idesc = kSwap ? idesc_bf16(kBM, p.np, p.a_mn != 0, false)
+                                          : idesc_bf16(kBM, kBN, false, p.b_mn != 0);
             int it = 0, lt = 0;
             bool ok = true;
             // descriptors advance by the k step: 32 bytes (2) along K for a
-            // K-major operand, 16 rows (2048 bytes, 128) for an N-major B
-            const uint64_t bstep = p.b_mn ? 128 : 2;
+            // K-major operand, 16 rows (2048 bytes, 128) for an M- or N-major one
+            const bool a_mn = kSwap && p.a_mn;
+            const bool b_mn = !kSwap && p.b_mn;
+            const uint64_t astep = a_mn ? 128 : 2;
+            const uint64_t bstep = b_mn ? 128 : 2;
             for (int t = blockIdx.x; t < num_items && ok; t += gridDim.x, ++lt) {
                 int tile, kt0, kt1;
                 item_range(t, p.splits, nk, &tile, &kt0, &kt1);
@@ -158,15 +220,17 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc(smem_u32(sA + s * kTileBytes), 16, 1024, 2);
-                    const uint64_t bd = p.b_mn
-                                            ? sdesc(smem_u32(sB + s * kTileBytes), kTileBytes / 2, 1024, 2)
-                                            : sdesc(smem_u32(sB + s * kTileBytes), 16, 1024, 2);
+                    const uint64_t ad = a_mn
+                                            ? sdesc(smem_u32(sA + s * kTileBytes), kTileBytes / 2, 1024, 2)
+                                            : sdesc(smem_u32(sA + s * kTileBytes), 16, 1024, 2);
+                    const uint64_t bd = b_mn
+                                            ? sdesc(smem_u32(sB + s * kBBytes), kTileBytes / 2, 1024, 2)
+                                            : sdesc(smem_u32(sB + s * kBBytes), 16, 1024, 2);
                     mma_ss(d, ad, bd, idesc, kt != kt0);
 #pragma unroll
                     for (int k = 1; k < kBK / 16; ++k)
                         asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d),
-                                     "l"(ad + 2 * k), "l"(bd + bstep * k), "r"(idesc)
+                                     "l"(ad + astep * k), "l"(bd + bstep * k), "r"(idesc)
                                      : "memory");
                     tc_commit(&empty[s]);
                 }
@@ -194,6 +258,25 @@ __global__ void __launch_bounds__(192, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            if (kSwap) {
+                // lane = output column n; TMEM columns = activation rows
+                const int n = n0 + row;
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kBN);
+                __nv_bfloat16* C = (__nv_bfloat16*)p.C + (int64_t)z * p.sCz + n;
+                for (int c = 0; c < p.np; c += 16) {
+                    uint32_t r[16];
+                    __syncwarp();
+                    MLA_TMEM_LD_X16(ta + (uint32_t)c, r);
+                    tmem_ld_wait();
+                    if (n >= p.N) continue;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (c + i < p.M) C[(int64_t)(c + i) * p.sCm] = __float2bfloat16_rn(__uint_as_float(r[i]));
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[ab]);
+                continue;
+            }
             int64_t slot = -1;
             if (p.splits == 1 && p.epi == 1 && m < p.M) {
                 const int b = p.seq_idx[m], ps = p.pos[m];
@@ -382,9 +465,9 @@ cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmP
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+                                             Ring<false>::smem);
         if (e != cudaSuccess) return e;
         attr[dev] = true;
     }
@@ -405,7 +488,7 @@ cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmP
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(192);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = Ring<false>::smem;
     cfg.stream = st;
     cudaLaunchAttribute la[1];
     la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -413,7 +496,7 @@ cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmP
     cfg.attrs = la;
     cfg.numAttrs = 1;
     cudaError_t e =
-        cudaLaunchKernelEx(&cfg, gemm_tc_kernel, ta, tb, p, tiles_n, tiles_m, (int)items);
+        cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false>, ta, tb, p, tiles_n, tiles_m, (int)items);
     if (e != cudaSuccess || p.splits == 1) return e;
     const int64_t threads = (int64_t)p.M * (p.N / 4);
     cudaLaunchConfig_t rc = {};
@@ -423,6 +506,55 @@ cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmP
     rc.attrs = la;
     rc.numAttrs = 1;
     return cudaLaunchKernelEx(&rc, splitk_reduce_kernel, p);
+}
+
+cudaError_t launch_gemm_tc_skinny(const TcOperand& X, const TcOperand& W, bool w_kn,
+                                  const TcGemmParams& pin, int batch, cudaStream_t st) {
+    TcGemmParams p = pin;
+    if (p.M <= 0 || p.M > kSkinnyMaxRows || p.N <= 0 || p.K <= 0 || batch <= 0 || p.epi != 0 ||
+        p.c_dtype != MLA_DTYPE_BF16)
+        return cudaErrorInvalidValue;
+    p.swap = 1;
+    p.a_mn = w_kn ? 1 : 0;
+    p.np = (p.M + 15) / 16 * 16;
+    p.splits = 1;
+    p.b_mn = 0;
+    CUtensorMap tw, tx;
+    const uint32_t boxWk[3] = {64, 128, 1};   // [n][k]: 128 columns x 64 k
+    const uint32_t boxWn[3] = {64, 64, 1};    // [k][n]: 64 k rows x 64 columns, twice
+    const uint32_t boxX[3] = {64, (uint32_t)p.np, 1};
+    if (!make_tmap_bf16(&tw, W.ptr, 3, W.dims, W.strides, w_kn ? boxWn : boxWk, 128) ||
+        !make_tmap_bf16(&tx, X.ptr, 3, X.dims, X.strides, boxX, 128))
+        return cudaErrorInvalidValue;
+    static bool attr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Ring<true>::smem);
+        if (e != cudaSuccess) return e;
+        attr[dev] = true;
+    }
+    static int sms[64] = {};
+    if (!sms[dev] &&
+        cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const int tiles_n = (p.N + kBM - 1) / kBM;
+    const int64_t items = (int64_t)tiles_n * batch;
+    if (items > 0x7fffffff) return cudaErrorInvalidValue;
+    const int grid = (int)(items < sms[dev] ? items : sms[dev]);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = Ring<true>::smem;
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, tw, tx, p, tiles_n, 1, (int)items);
 }
 
 }  // namespace mla

@@ -126,10 +126,21 @@ struct TcGemmParams {
     float* partial;
     size_t partial_bytes;
     int splits;
+    // skinny products (M <= 64, batched over z): the weights are the MMA's
+    // A operand (128 output columns per tile as TMEM lanes) and the M rows of
+    // activations its B operand, padded to np rows; set by
+    // launch_gemm_tc_skinny
+    int swap;
+    int a_mn;              // swap: weights stored [k][n]
+    int np;
 };
 
 cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmParams& p,
                            int batch, cudaStream_t st);
+// The same product C[z] = X[z] W[z] for few rows (M <= 64): X is [M][K]
+// (K-major), W is [N][K] (w_kn = false) or [K][N] (w_kn = true); bf16 C.
+cudaError_t launch_gemm_tc_skinny(const TcOperand& X, const TcOperand& W, bool w_kn,
+                                  const TcGemmParams& p, int batch, cudaStream_t st);
 // fp32 scratch bytes with which launch_gemm_tc would split a batch-1 M x N x K
 // product over `sms` SMs (0: it would not split).
 size_t gemm_tc_split_scratch(int M, int N, int K, int sms);

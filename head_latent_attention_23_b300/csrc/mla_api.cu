@@ -89,6 +89,10 @@ int decode_workers(const mla_config* c, int batch, int* W) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Per-head products with at most this many rows run transposed (weights as
+// the MMA's 128-row side): the rows would otherwise fill a small part of it.
+constexpr int kSkinnyRows = 64;
+
 bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 // 3-D bf16 operand view for the tensor-core GEMM.
@@ -251,6 +255,7 @@ int mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* w_uk, in
         TcOperand B = op3(w_uk, DN, DL, H, (uint64_t)DN * 2, (uint64_t)DL * DN * 2);
         TcGemmParams g = gemm_params(batch, DL, DN, false, q_lat, DL, (int64_t)H * DL,
                                      MLA_DTYPE_BF16, status);
+        if (batch <= kSkinnyRows) return cuda_rc(launch_gemm_tc_skinny(A, B, false, g, H, st));
         return cuda_rc(launch_gemm_tc(A, B, g, H, st));
     }
     // per head h: q_lat[:, h, :] (batch x DL) = q_nope[:, h, :] (batch x DN) . W_LK_h^T
@@ -379,7 +384,9 @@ int project_out_impl(const mla_config* cfg, const void* o_lat, const void* w_uv,
         TcOperand B = op3(w_uv, DV, DL, H, (uint64_t)DV * 2, (uint64_t)DL * DV * 2);
         TcGemmParams g = gemm_params(batch, DV, DL, true, o_v, DV, (int64_t)H * DV,
                                      MLA_DTYPE_BF16, status);
-        if (int rc = cuda_rc(launch_gemm_tc(A, B, g, H, st))) return rc;
+        if (int rc = cuda_rc(batch <= kSkinnyRows ? launch_gemm_tc_skinny(A, B, true, g, H, st)
+                                                  : launch_gemm_tc(A, B, g, H, st)))
+            return rc;
         if (!w_o) return MLA_OK;
         const uint64_t KO = (uint64_t)H * DV;
         TcOperand A2 = op3(o_v, KO, batch, 1, KO * 2, KO * 2 * batch);
