@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(192, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = (p.K + kBK - 1) / kBK;
-    int pre = 0;    // skinny: slices whose weight copies went out before the wait
+    int pre = 0;    // slices whose weight copies went out before the wait
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -113,13 +113,16 @@ __global__ void __launch_bounds__(192, 1)
         fence_mbar_init();
         prefetch_tmap(&tA);
         prefetch_tmap(&tB);
-        if (kSwap) {
-            // No kernel this one may overlap writes the weights, so the first
-            // stages' weight slices are requested before the previous kernel
-            // has finished: their first-touch latency hides behind its tail.
-            for (int t = blockIdx.x; t < num_items && pre < kStages; t += gridDim.x) {
-                const TileId ti = tile_of(t, tiles_n, tiles_m);
-                for (int kt = 0; kt < nk && pre < kStages; ++kt, ++pre) {
+        // The weights (B, or A of a skinny product) are never written by a
+        // kernel this one may overlap, so the first stages' weight slices are
+        // requested before the previous kernel has finished: their
+        // first-touch latency hides behind its tail.
+        for (int t = blockIdx.x; t < num_items && pre < kStages; t += gridDim.x) {
+            int tile, kt0, kt1;
+            item_range(t, p.splits, nk, &tile, &kt0, &kt1);
+            const TileId ti = tile_of(tile, tiles_n, tiles_m);
+            for (int kt = kt0; kt < kt1 && pre < kStages; ++kt, ++pre) {
+                if (kSwap) {
                     uint8_t* dst = sA + pre * kTileBytes;
                     mbar_arrive_expect_tx(&full[pre], kTileBytes + p.np * 128);
                     if (p.a_mn) {
@@ -128,6 +131,16 @@ __global__ void __launch_bounds__(192, 1)
                                     &full[pre]);
                     } else {
                         tma_load_3d(dst, &tA, kt * kBK, ti.n0, ti.z, &full[pre]);
+                    }
+                } else {
+                    uint8_t* dst = sB + pre * kBBytes;
+                    mbar_arrive_expect_tx(&full[pre], 2 * kTileBytes);
+                    if (p.b_mn) {
+                        tma_load_3d(dst, &tB, ti.n0, kt * kBK, ti.z, &full[pre]);
+                        tma_load_3d(dst + kTileBytes / 2, &tB, ti.n0 + 64, kt * kBK, ti.z,
+                                    &full[pre]);
+                    } else {
+                        tma_load_3d(dst, &tB, kt * kBK, ti.n0, ti.z, &full[pre]);
                     }
                 }
             }
@@ -155,9 +168,12 @@ __global__ void __launch_bounds__(192, 1)
                 const TileId ti = tile_of(tile, tiles_n, tiles_m);
                 for (int kt = kt0; kt < kt1; ++kt, ++it) {
                     const int s = it % kStages;
-                    if (kSwap && it < pre) {
+                    if (it < pre) {
                         // weights requested before the wait: the activations now
-                        tma_load_3d(sB + s * kBBytes, &tB, kt * kBK, 0, ti.z, &full[s]);
+                        if (kSwap)
+                            tma_load_3d(sB + s * kBBytes, &tB, kt * kBK, 0, ti.z, &full[s]);
+                        else
+                            tma_load_3d(sA + s * kTileBytes, &tA, kt * kBK, ti.m0, ti.z, &full[s]);
                         continue;
                     }
                     if (!mbar_wait_fast(&empty[s], ((it / kStages) & 1) ^ 1, abort_flag,

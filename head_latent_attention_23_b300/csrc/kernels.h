@@ -135,6 +135,9 @@ struct TcGemmParams {
     int np;
 };
 
+// B must be weights: nothing that may run concurrently (the previous kernel
+// on the stream, under programmatic dependent launch) writes it, because its
+// first slices are read before the wait for that kernel.
 cudaError_t launch_gemm_tc(const TcOperand& A, const TcOperand& B, const TcGemmParams& p,
                            int batch, cudaStream_t st);
 // The same product C[z] = X[z] W[z] for few rows (M <= 64): X is [M][K]
