@@ -5,8 +5,9 @@
 // is L = X W_L, one d_latent row per token for all heads; "The RoPE problem":
 // a separate non-latent key part carries the rotary embedding.  The rotation
 // convention (a reading; the pages give no formula): pairs (2j, 2j+1) turn by
-// pos * rope_base^(-2j/d_rope).  Angles are formed and reduced in fp64 so
-// positions near 1e5 keep full fp32 accuracy after the rotation.
+// pos * rope_base^(-2j/d_rope).  Angles are formed and reduced to [-pi, pi]
+// in fp64 (rope_cos_sin), so positions near 1e5 keep full fp32 accuracy
+// after the rotation.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -40,11 +41,8 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     const int p = a.pos[t];
     // rotary part: thread j < d_rope/2 rotates pair j
     for (int j = tid; j < a.d_rope / 2; j += blockDim.x) {
-        double theta = pow(a.rope_base, -2.0 * (double)j / (double)a.d_rope);
-        double phi = fmod((double)p * theta, 6.283185307179586476925286766559);
-        double sn, cs;
-        sincos(phi, &sn, &cs);
-        float c = (float)cs, s = (float)sn;
+        float c, s;
+        rope_cos_sin(a.rope_theta1, j, p, &c, &s);
         float x0 = row[a.d_latent + 2 * j], x1 = row[a.d_latent + 2 * j + 1];
         row[a.d_latent + 2 * j] = x0 * c - x1 * s;
         row[a.d_latent + 2 * j + 1] = x0 * s + x1 * c;
@@ -85,57 +83,84 @@ cudaError_t launch_append(const AppendArgs& a, int dtype, cudaStream_t st) {
 
 // ---------------------------------------------------------------- queries
 // q_all [batch][heads][d_nope + d_rope] fp32 -> q_nope (copy) and q_pe
-// (rotated at the sequence's position), both in dtype.  One CTA per
-// sequence: the rotation angles depend only on the position, so each pair's
-// cosine and sine are formed once per sequence (in fp64, then rounded to
-// fp32) and shared by all heads; fp64 transcendentals are slow on this GPU.
+// (rotated at the sequence's position), both in dtype.  A CTA takes one
+// sequence and kQHeads heads: the rotation angles depend only on the
+// position, so each pair's cosine and sine are formed once per CTA and shared
+// by its heads.  Threads move element pairs (8-byte loads) and each does a
+// few of them, so the many CTAs, not a long per-thread loop, hide the memory
+// latency.
+constexpr int kQHeads = 16;
+
+template <typename T>
+__device__ __forceinline__ void store_pair(T* dst, float a, float b);
+template <>
+__device__ __forceinline__ void store_pair<float>(float* dst, float a, float b) {
+    *(float2*)dst = make_float2(a, b);
+}
+template <>
+__device__ __forceinline__ void store_pair<__nv_bfloat16>(__nv_bfloat16* dst, float a, float b) {
+    *(__nv_bfloat162*)dst = __floats2bfloat162_rn(a, b);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) q_split_rope_kernel(
     const float* __restrict__ q_all, int heads, int d_nope, int d_rope,
-    const int32_t* __restrict__ pos, double rope_base, T* __restrict__ q_nope,
+    const int32_t* __restrict__ pos, double rope_theta1, T* __restrict__ q_nope,
     T* __restrict__ q_pe) {
     extern __shared__ float cs[];   // [d_rope / 2][2]: cos, sin
-    const int b = blockIdx.x, half_r = d_rope / 2;
+    const int b = blockIdx.x, h0 = blockIdx.y * kQHeads, half_r = d_rope / 2;
+    const int hn = min(kQHeads, heads - h0);
     const int p = pos[b];
-    for (int j = threadIdx.x; j < half_r; j += blockDim.x) {
-        const double theta = pow(rope_base, -2.0 * (double)j / (double)d_rope);
-        const double phi = fmod((double)p * theta, 6.283185307179586476925286766559);
-        double sn, c;
-        sincos(phi, &sn, &c);
-        cs[2 * j] = (float)c;
-        cs[2 * j + 1] = (float)sn;
-    }
+    for (int j = threadIdx.x; j < half_r; j += blockDim.x)
+        rope_cos_sin(rope_theta1, j, p, &cs[2 * j], &cs[2 * j + 1]);
     __syncthreads();
     const int dq = d_nope + d_rope;
-    const float* src = q_all + (size_t)b * heads * dq;
-    T* dn = q_nope + (size_t)b * heads * d_nope;
-    T* dp = q_pe + (size_t)b * heads * d_rope;
-    for (int e = threadIdx.x; e < heads * d_nope; e += blockDim.x) {
-        const int h = e / d_nope, j = e - h * d_nope;
-        dn[e] = from_f<T>(src[(size_t)h * dq + j]);
-    }
-    for (int e = threadIdx.x; e < heads * half_r; e += blockDim.x) {
-        const int h = e / half_r, j = e - h * half_r;
-        const float x0 = src[(size_t)h * dq + d_nope + 2 * j];
-        const float x1 = src[(size_t)h * dq + d_nope + 2 * j + 1];
-        const float c = cs[2 * j], s = cs[2 * j + 1];
-        dp[(size_t)h * d_rope + 2 * j] = from_f<T>(x0 * c - x1 * s);
-        dp[(size_t)h * d_rope + 2 * j + 1] = from_f<T>(x0 * s + x1 * c);
+    const float* src = q_all + ((size_t)b * heads + h0) * dq;
+    T* dn = q_nope + ((size_t)b * heads + h0) * d_nope;
+    T* dp = q_pe + ((size_t)b * heads + h0) * d_rope;
+    if ((d_nope & 1) == 0) {
+        const int half_n = d_nope / 2;
+        for (int e = threadIdx.x; e < hn * half_n; e += blockDim.x) {
+            const int h = e / half_n, j = 2 * (e - h * half_n);
+            const float2 v = *(const float2*)(src + (size_t)h * dq + j);
+            store_pair<T>(dn + (size_t)h * d_nope + j, v.x, v.y);
+        }
+        for (int e = threadIdx.x; e < hn * half_r; e += blockDim.x) {
+            const int h = e / half_r, j = e - h * half_r;
+            const float2 x = *(const float2*)(src + (size_t)h * dq + d_nope + 2 * j);
+            const float c = cs[2 * j], sn = cs[2 * j + 1];
+            store_pair<T>(dp + (size_t)h * d_rope + 2 * j, x.x * c - x.y * sn, x.x * sn + x.y * c);
+        }
+    } else {
+        // odd d_nope: rows are not 8-byte aligned, move single elements
+        for (int e = threadIdx.x; e < hn * d_nope; e += blockDim.x) {
+            const int h = e / d_nope, j = e - h * d_nope;
+            dn[(size_t)h * d_nope + j] = from_f<T>(src[(size_t)h * dq + j]);
+        }
+        for (int e = threadIdx.x; e < hn * half_r; e += blockDim.x) {
+            const int h = e / half_r, j = e - h * half_r;
+            const float x0 = src[(size_t)h * dq + d_nope + 2 * j];
+            const float x1 = src[(size_t)h * dq + d_nope + 2 * j + 1];
+            const float c = cs[2 * j], sn = cs[2 * j + 1];
+            dp[(size_t)h * d_rope + 2 * j] = from_f<T>(x0 * c - x1 * sn);
+            dp[(size_t)h * d_rope + 2 * j + 1] = from_f<T>(x0 * sn + x1 * c);
+        }
     }
 }
 
 cudaError_t launch_q_split_rope(const float* q_all, int batch, int heads, int d_nope,
-                                int d_rope, const int32_t* pos, double rope_base, void* q_nope,
+                                int d_rope, const int32_t* pos, double rope_theta1, void* q_nope,
                                 void* q_pe, int dtype, cudaStream_t st) {
     const size_t sm = (size_t)(d_rope > 0 ? d_rope : 2) * sizeof(float);
+    const dim3 grid(batch, (heads + kQHeads - 1) / kQHeads);
     if (dtype == MLA_DTYPE_BF16)
-        q_split_rope_kernel<__nv_bfloat16><<<batch, 256, sm, st>>>(
-            q_all, heads, d_nope, d_rope, pos, rope_base, (__nv_bfloat16*)q_nope,
+        q_split_rope_kernel<__nv_bfloat16><<<grid, 256, sm, st>>>(
+            q_all, heads, d_nope, d_rope, pos, rope_theta1, (__nv_bfloat16*)q_nope,
             (__nv_bfloat16*)q_pe);
     else
-        q_split_rope_kernel<float><<<batch, 256, sm, st>>>(q_all, heads, d_nope, d_rope, pos,
-                                                          rope_base, (float*)q_nope,
-                                                          (float*)q_pe);
+        q_split_rope_kernel<float><<<grid, 256, sm, st>>>(q_all, heads, d_nope, d_rope, pos,
+                                                         rope_theta1, (float*)q_nope,
+                                                         (float*)q_pe);
     return cudaGetLastError();
 }
 

@@ -59,6 +59,27 @@ __host__ __device__ __forceinline__ int64_t plan_lo(int g, int64_t total, int W)
 }
 
 // Seq length actually used: out-of-range lengths are flagged and clamped.
+// Rotation of RoPE pair j at position pos, as (cos, sin) in fp32.  The
+// frequency theta_j = theta1^j comes from theta1 = rope_base^(-2/d_rope)
+// (formed in fp64 on the host) by repeated squaring in fp64; the angle
+// pos * theta_j is formed in fp64 and reduced to about [-pi, pi] by
+// subtracting the nearest multiple of 2 pi, with 2 pi split into two
+// doubles (Cody and Waite's reduction), so positions near 1e5 keep the
+// angle's fp32 accuracy; sincosf then takes the small reduced angle.  Only
+// multiplies and fused multiply-adds run in fp64, which is slow on this GPU.
+__device__ __forceinline__ void rope_cos_sin(double theta1, int j, int pos, float* c, float* s) {
+    double th = 1.0, b = theta1;
+    for (int e = j; e; e >>= 1) {
+        if (e & 1) th *= b;
+        b *= b;
+    }
+    const double phi = (double)pos * th;
+    const double k = rint(phi * 0.15915494309189535);     // nearest turn: phi / (2 pi)
+    double r = fma(-k, 6.283185307179586, phi);           // 2 pi, leading double
+    r = fma(-k, 2.4492935982947064e-16, r);               // 2 pi, remainder
+    sincosf((float)r, s, c);
+}
+
 __device__ __forceinline__ int clamp_len(int n, int cap, int* status) {
     if (n < 1 || n > cap) {
         flag(status, MLA_ERR_INVALID_ARG);

@@ -332,14 +332,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                         for (int i = 0; i < 16; i += 2) {
                             const int j = (nb + i - p.d_latent) / 2;
-                            const double theta = pow(p.rope_base, -2.0 * j / (double)p.d_rope);
-                            const double phi =
-                                fmod((double)ps * theta, 6.283185307179586476925286766559);
-                            double sn, cs;
-                            sincos(phi, &sn, &cs);
+                            float cs, sn;
+                            rope_cos_sin(p.rope_theta1, j, ps, &cs, &sn);
                             const float x0 = v[i], x1 = v[i + 1];
-                            v[i] = x0 * (float)cs - x1 * (float)sn;
-                            v[i + 1] = x0 * (float)sn + x1 * (float)cs;
+                            v[i] = x0 * cs - x1 * sn;
+                            v[i + 1] = x0 * sn + x1 * cs;
                         }
                     }
                     const int D = p.N;
@@ -397,8 +394,21 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcGemmParams p
     if (idx < (int64_t)p.M * n4) {
         const int m = (int)(idx / n4), n = (int)(idx % n4) * 4;
         float v[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int sp = 0; sp < p.splits; ++sp) {
-            const float4 x = *(const float4*)(p.partial + ((size_t)sp * p.M + m) * p.N + n);
+        const float* part = p.partial + (size_t)m * p.N + n;
+        const size_t sstride = (size_t)p.M * p.N;
+        // four partials' loads in flight at a time; the sum keeps split order
+        int sp = 0;
+        for (; sp + 4 <= p.splits; sp += 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = *(const float4*)(part + (size_t)(sp + u) * sstride);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                v[0] += x[u].x; v[1] += x[u].y; v[2] += x[u].z; v[3] += x[u].w;
+            }
+        }
+        for (; sp < p.splits; ++sp) {
+            const float4 x = *(const float4*)(part + (size_t)sp * sstride);
             v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
         }
         if (p.epi == 1) {
@@ -414,13 +424,11 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcGemmParams p
 #pragma unroll
                 for (int i = 0; i < 4; i += 2) {
                     const int j = (n + i - p.d_latent) / 2;
-                    const double theta = pow(p.rope_base, -2.0 * j / (double)p.d_rope);
-                    const double phi = fmod((double)ps * theta, 6.283185307179586476925286766559);
-                    double sn, cs;
-                    sincos(phi, &sn, &cs);
+                    float cs, sn;
+                    rope_cos_sin(p.rope_theta1, j, ps, &cs, &sn);
                     const float x0 = v[i], x1 = v[i + 1];
-                    v[i] = x0 * (float)cs - x1 * (float)sn;
-                    v[i + 1] = x0 * (float)sn + x1 * (float)cs;
+                    v[i] = x0 * cs - x1 * sn;
+                    v[i + 1] = x0 * sn + x1 * cs;
                 }
             }
             uint2 w;

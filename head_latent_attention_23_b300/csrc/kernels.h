@@ -52,7 +52,7 @@ cudaError_t launch_combine_dense(const float* o_part, const float* lse_part, int
 struct AppendArgs {
     int n_tok, d_in, d_latent, d_rope, block_size, max_blocks, batch;
     int64_t num_blocks;
-    double rope_base;
+    double rope_theta1;     // rope_base^(-2 / d_rope): the first pair's frequency
     const void* x;          // [n_tok][d_in]
     const void* w_dkv;      // [d_in][d_latent + d_rope]
     const int32_t* seq_idx;
@@ -81,7 +81,7 @@ cudaError_t launch_gemm_simt(const GemmArgs& g, int a_dtype, int b_dtype, int c_
 // Splits fp32 per-head query rows [batch][heads][d_nope + d_rope] into
 // q_nope and the rotated q_pe (dtype).
 cudaError_t launch_q_split_rope(const float* q_all, int batch, int heads, int d_nope,
-                                int d_rope, const int32_t* pos, double rope_base, void* q_nope,
+                                int d_rope, const int32_t* pos, double rope_theta1, void* q_nope,
                                 void* q_pe, int dtype, cudaStream_t st);
 
 // Multi-token decode rows: lens_x[b * T + j] = seq_lens[b] - T + 1 + j and a
@@ -114,7 +114,7 @@ struct TcGemmParams {
     // epi 1: rows are tokens, columns [0, d_latent) latent, [d_latent, N) rotary
     int d_latent, d_rope, block_size, max_blocks, batch;
     int64_t num_blocks;
-    double rope_base;
+    double rope_theta1;    // rope_base^(-2 / d_rope)
     const int32_t* seq_idx;
     const int32_t* pos;
     const int32_t* block_table;

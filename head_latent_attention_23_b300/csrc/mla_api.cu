@@ -70,6 +70,12 @@ int check_cfg(const mla_config* c) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
+// Frequency of the first RoPE pair, rope_base^(-2 / d_rope); pair j turns
+// by theta1^j per position (interleaved pairs, theta_j = base^(-2j/d_rope)).
+double rope_theta1(const mla_config* c) {
+    return c->d_rope > 0 ? pow(c->rope_base, -2.0 / (double)c->d_rope) : 1.0;
+}
+
 constexpr int kMaxDecodeBatch = 8192;
 
 // The tensor-core kernel takes the maximum of the raw scores, which needs a
@@ -214,7 +220,7 @@ int append_latent_impl(const mla_config* cfg, const void* x, int n_tok, int d_in
         g.epi = 1;
         g.d_latent = cfg->d_latent; g.d_rope = cfg->d_rope; g.block_size = cfg->block_size;
         g.max_blocks = max_blocks; g.batch = batch; g.num_blocks = num_blocks;
-        g.rope_base = cfg->rope_base; g.seq_idx = seq_idx; g.pos = pos;
+        g.rope_theta1 = rope_theta1(cfg); g.seq_idx = seq_idx; g.pos = pos;
         g.block_table = block_table; g.cache = (__nv_bfloat16*)cache;
         g.dense_out = (__nv_bfloat16*)dense_out;
         return cuda_rc(launch_gemm_tc(A, B, g, 1, (cudaStream_t)stream));
@@ -222,7 +228,7 @@ int append_latent_impl(const mla_config* cfg, const void* x, int n_tok, int d_in
     AppendArgs a{};
     a.n_tok = n_tok; a.d_in = d_in; a.d_latent = cfg->d_latent; a.d_rope = cfg->d_rope;
     a.block_size = cfg->block_size; a.max_blocks = max_blocks; a.batch = batch;
-    a.num_blocks = num_blocks; a.rope_base = cfg->rope_base; a.x = x; a.w_dkv = w_dkv;
+    a.num_blocks = num_blocks; a.rope_theta1 = rope_theta1(cfg); a.x = x; a.w_dkv = w_dkv;
     a.seq_idx = seq_idx; a.pos = pos; a.block_table = block_table; a.cache = cache;
     a.dense_out = dense_out; a.rows_f32 = nullptr; a.status = status;
     return cuda_rc(launch_append(a, cfg->dtype, (cudaStream_t)stream));
@@ -471,7 +477,7 @@ int query_proj_impl(const mla_config* cfg, const void* x, int batch, int d_in, c
                                      MLA_DTYPE_F32, status, sp);
         if (int rc = cuda_rc(launch_gemm_tc(A, B, g, 1, st))) return rc;
         return cuda_rc(launch_q_split_rope(q_all, batch, H, cfg->d_nope, cfg->d_rope, pos,
-                                           cfg->rope_base, q_nope, q_pe, cfg->dtype, st));
+                                           rope_theta1(cfg), q_nope, q_pe, cfg->dtype, st));
     }
     const void* a_in = x;
     int a_dtype = cfg->dtype, k_in = d_in;
@@ -492,7 +498,7 @@ int query_proj_impl(const mla_config* cfg, const void* x, int batch, int d_in, c
     u.C = q_all; u.sCm = (int64_t)H * DQ; u.sCn = 1;
     if (int rc = cuda_rc(launch_gemm_simt(u, a_dtype, cfg->dtype, MLA_DTYPE_F32, st))) return rc;
     return cuda_rc(launch_q_split_rope(q_all, batch, H, cfg->d_nope, cfg->d_rope, pos,
-                                       cfg->rope_base, q_nope, q_pe, cfg->dtype, st));
+                                       rope_theta1(cfg), q_nope, q_pe, cfg->dtype, st));
 }
 
 }  // namespace
