@@ -355,7 +355,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             };
             for (int k = 0; k < K && ok; ++k, cur.next()) {
                 const int t0 = cur.tile_in_seq() * kT;
-                const TileRows tr = tile_rows(a, cur.b, lens[cur.b], t0, scorer);
                 if (scorer) {
                     if (cur.first(lo)) {
                         // the range's query: the rotary part into its own buffer
@@ -391,6 +390,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         if (!ok) break;
                     }
+                    // the tile's pages: a block-table read, issued after the
+                    // range's query copies so that their latency covers it
+                    const TileRows tr = tile_rows(a, cur.b, lens[cur.b], t0, true);
                     // the two pages of the tile in one 128-row box when they are
                     // adjacent in the pool (fewer, larger TMA requests), else one
                     // 64-row box each; the shared-memory image is the same
@@ -412,6 +414,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
+                    const TileRows tr = tile_rows(a, cur.b, lens[cur.b], t0, false);
                     // one box per chunk: 64 rows of a page x four 64-column
                     // groups.  This is the last read of these rows: their L2
                     // lines go first, ahead of the partials, queries and weights
