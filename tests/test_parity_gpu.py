@@ -76,6 +76,22 @@ def test_decode_small_ragged_bf16(lens, permute):
         assert rel(host(res[key]), ref[key]) <= TOL["bf16"], key
 
 
+@pytest.mark.parametrize("batch", [1, 15, 17, 64, 65])
+def test_projection_modes_around_the_skinny_limit(batch):
+    """The per-head absorb and value projections run transposed (weights as
+    the MMA's 128-row side) up to 64 rows and tiled above; batch sizes on both
+    sides of the limit and of the 16-row padding, every (sequence, head) pair
+    of q_lat-dependent o_lat, lse and o_v against the oracle."""
+    g = torch.Generator().manual_seed(batch)
+    lens = torch.randint(1, 200, (batch,), generator=g).tolist()
+    w = W.cached_decode(batch, lens, seed=60 + batch, permute=True)
+    step = run_step(w)
+    ref = O.reference_cached_decode(W.oracle_view(w))
+    res = step.results()
+    for key in ("o_lat", "o_v", "lse"):
+        assert rel(host(res[key]), ref[key]) <= TOL["bf16"], key
+
+
 def test_seq_len_one_returns_the_cached_latent():
     w = W.cached_decode(3, [1, 1, 1], seed=5, permute=True)
     step = run_step(w)
