@@ -37,13 +37,14 @@ namespace {
 
 constexpr int kBM = 128, kBN = 128, kBK = 64;
 constexpr int kTileBytes = 16384;   // one 128 x 64 bf16 slice of A or of B
-// Ring: four stages of A and B slices; a skinny product's stage is a weight
-// slice and at most 64 activation rows (8 KB), so seven stages fit (next to
-// two CTAs of the merge kernel, which it may overlap) and most of a CTA's
-// share of the weights is in flight at once.
+// Ring: six stages of A and B slices (96 KB of weights in flight per SM:
+// with HBM latency near 2 us under load, fewer stages cap a CTA's weight
+// stream below its share of the bandwidth); a skinny product's stage is a
+// weight slice and at most 64 activation rows (8 KB), so seven stages fit
+// next to two CTAs of the merge kernel, which it may overlap.
 template <bool kSwap>
 struct Ring {
-    static constexpr int stages = kSwap ? 7 : 4;
+    static constexpr int stages = kSwap ? 7 : 6;
     static constexpr int b_bytes = kSwap ? 8192 : kTileBytes;
     static constexpr int smem = 1024 + stages * (kTileBytes + b_bytes) + 256;
 };
