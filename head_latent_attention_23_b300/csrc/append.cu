@@ -201,6 +201,25 @@ cudaError_t launch_expand_rows(const int32_t* seq_lens, const int32_t* block_tab
     return cudaGetLastError();
 }
 
+// (cos, sin) of every RoPE pair at each sequence's position, for epilogues
+// that rotate many heads' query parts: formed once per (sequence, pair).
+__global__ void rope_table_kernel(const int32_t* __restrict__ pos, int half_r, double rope_theta1,
+                                  float2* __restrict__ table) {
+    const int b = blockIdx.x, p = pos[b];
+    for (int j = threadIdx.x; j < half_r; j += blockDim.x) {
+        float c, s;
+        rope_cos_sin(rope_theta1, j, p, &c, &s);
+        table[(size_t)b * half_r + j] = make_float2(c, s);
+    }
+}
+
+cudaError_t launch_rope_table(const int32_t* pos, int batch, int d_rope, double rope_theta1,
+                              float2* table, cudaStream_t st) {
+    if (d_rope < 2) return cudaSuccess;
+    rope_table_kernel<<<batch, 32, 0, st>>>(pos, d_rope / 2, rope_theta1, table);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_step_positions(const int32_t* seq_lens, int batch, int32_t* pos,
                                   int32_t* seq_idx, cudaStream_t st) {
     step_positions_kernel<<<(batch + 255) / 256, 256, 0, st>>>(seq_lens, batch, pos, seq_idx);

@@ -54,6 +54,26 @@ constexpr int kAcc = 2;             // TMEM accumulators: the epilogue drains on
 
 using namespace tc;
 
+// Query split epilogue (epi 2): columns (n, n + 1) of row m, n even, are a
+// pair of head n / (d_nope + d_rope): the latent-side part goes to q_nope as
+// is, the rotary part is rotated by the row's (cos, sin) from p.rope_cs and
+// goes to q_pe (one rounding to bf16 after fp32 sums and the rotation).
+__device__ __forceinline__ void query_pair(const TcGemmParams& p, int m, int n, float x0,
+                                           float x1) {
+    const int dq = p.d_nope + p.d_rope, hq = p.N / dq;
+    const int h = n / dq, j = n - h * dq;
+    if (j < p.d_nope) {
+        *(__nv_bfloat162*)(p.q_nope + ((size_t)m * hq + h) * p.d_nope + j) =
+            __floats2bfloat162_rn(x0, x1);
+    } else {
+        const int jr = (j - p.d_nope) >> 1;
+        const float2 r = p.rope_cs[(size_t)m * (p.d_rope >> 1) + jr];
+        const float cs = r.x, sn = r.y;
+        *(__nv_bfloat162*)(p.q_pe + ((size_t)m * hq + h) * p.d_rope + 2 * jr) =
+            __floats2bfloat162_rn(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+    }
+}
+
 // Output tile `t` of the (n, m, z) grid of 128 x 128 tiles.
 struct TileId {
     int n0, m0, z;
@@ -326,6 +346,11 @@ __global__ void __launch_bounds__(192, 1)
                         for (int i = 0; i < 16; ++i)
                             if (nb + i < p.N) P[i] = v[i];
                     }
+                } else if (p.epi == 2) {
+                    if (nb >= p.N) continue;
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2)
+                        if (nb + i < p.N) query_pair(p, m, nb + i, v[i], v[i + 1]);
                 } else if (p.epi == 1) {
                     if (nb >= p.N) continue;
                     if (nb >= p.d_latent) {
@@ -412,7 +437,10 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcGemmParams p
             const float4 x = *(const float4*)(part + (size_t)sp * sstride);
             v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
         }
-        if (p.epi == 1) {
+        if (p.epi == 2) {
+            query_pair(p, m, n, v[0], v[1]);
+            query_pair(p, m, n + 2, v[2], v[3]);
+        } else if (p.epi == 1) {
             int64_t slot = -1;
             const int b = p.seq_idx[m], ps = p.pos[m];
             if (b >= 0 && b < p.batch && ps >= 0 && ps < p.max_blocks * p.block_size) {

@@ -30,6 +30,10 @@ struct DecodeArgs {
     uint64_t wait_ns;       // give-up time of the tensor-core kernel's pipeline waits
 };
 
+// (cos, sin) of every RoPE pair at each sequence's position: table[b][j].
+cudaError_t launch_rope_table(const int32_t* pos, int batch, int d_rope, double rope_theta1,
+                              float2* table, cudaStream_t st);
+
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t st);
 size_t decode_simt_smem(const DecodeArgs& a);
 
@@ -107,12 +111,19 @@ struct TcOperand {
 struct TcGemmParams {
     int M, N, K;
     int b_mn;              // 1: B stored [k][n]
-    int epi;               // 0: store C; 1: cache append (RoPE + paged scatter)
+    int epi;               // 0: store C; 1: cache append (RoPE + paged scatter);
+                           // 2: query split (columns of head h: d_nope to q_nope,
+                           //    d_rope rotated at pos[m] to q_pe; bf16)
     void* C;               // epi 0: element (z, m, n) at C + z*sCz + m*sCm + n
     int64_t sCz, sCm;
     int c_dtype;
     // epi 1: rows are tokens, columns [0, d_latent) latent, [d_latent, N) rotary
     int d_latent, d_rope, block_size, max_blocks, batch;
+    // epi 2: rows are sequences, N = heads x (d_nope + d_rope)
+    int d_nope;
+    __nv_bfloat16* q_nope;  // [M][heads][d_nope]
+    __nv_bfloat16* q_pe;    // [M][heads][d_rope]
+    const float2* rope_cs;  // [M][d_rope / 2] (cos, sin) at each row's position
     int64_t num_blocks;
     double rope_theta1;    // rope_base^(-2 / d_rope)
     const int32_t* seq_idx;

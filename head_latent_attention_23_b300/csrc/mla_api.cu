@@ -459,6 +459,15 @@ int query_proj_impl(const mla_config* cfg, const void* x, int batch, int d_in, c
         if (int rc = status_ptr(&status)) return rc;
         const void* a_in = x;
         int k_in = d_in;
+        // the query split and rotation run in W_UQ's epilogue when the halves
+        // of a head's columns are whole bf16 pairs; the rotations' (cos, sin)
+        // are formed once per (sequence, pair) into the scratch, first, since
+        // they depend only on the positions
+        const bool fused = cfg->d_nope % 2 == 0 && al16(q_nope) && (cfg->d_rope == 0 || al16(q_pe));
+        float2* rope_cs = (float2*)q_all;
+        if (fused &&
+            launch_rope_table(pos, batch, cfg->d_rope, rope_theta1(cfg), rope_cs, st) != cudaSuccess)
+            return MLA_ERR_CUDA;
         if (w_dq) {
             // c_q = x . W_DQ, kept in bf16 (scratch) as the next GEMM's A operand
             TcOperand A = op3(x, d_in, batch, 1, (uint64_t)d_in * 2, (uint64_t)d_in * 2 * batch);
@@ -473,6 +482,17 @@ int query_proj_impl(const mla_config* cfg, const void* x, int batch, int d_in, c
         const uint64_t NQ = (uint64_t)H * DQ;
         TcOperand A = op3(a_in, k_in, batch, 1, (uint64_t)k_in * 2, (uint64_t)k_in * 2 * batch);
         TcOperand B = op3(w_uq, NQ, k_in, 1, NQ * 2, NQ * 2 * k_in);
+        if (fused) {
+            TcGemmParams g = gemm_params(batch, (int)NQ, k_in, true, nullptr, 0, 0,
+                                         MLA_DTYPE_BF16, status, sp);
+            g.epi = 2;
+            g.d_nope = cfg->d_nope;
+            g.d_rope = cfg->d_rope;
+            g.q_nope = (__nv_bfloat16*)q_nope;
+            g.q_pe = (__nv_bfloat16*)q_pe;
+            g.rope_cs = rope_cs;
+            return cuda_rc(launch_gemm_tc(A, B, g, 1, st));
+        }
         TcGemmParams g = gemm_params(batch, (int)NQ, k_in, true, q_all, 0, (int64_t)NQ,
                                      MLA_DTYPE_F32, status, sp);
         if (int rc = cuda_rc(launch_gemm_tc(A, B, g, 1, st))) return rc;

@@ -157,7 +157,9 @@ class DecodeStep:
         if self.kind == "multi":
             n += 1                          # per-token rows of the split plan
         if self.kind == "token":
-            n += (2 if self.w_dq is not None else 1) + 1   # query GEMM(s) + split/rope
+            n += 2 if self.w_dq is not None else 1   # query GEMM(s)
+            n += 1                          # split/rotate kernel, or (bf16) the rotation table
+                                            # for the split fused into W_UQ's epilogue
             n += 1                          # append
             n += 1                          # W_O
             if fused:
