@@ -58,7 +58,6 @@ __host__ __device__ __forceinline__ int64_t plan_lo(int g, int64_t total, int W)
     return (int64_t)g * total / W;
 }
 
-// Seq length actually used: out-of-range lengths are flagged and clamped.
 // Rotation of RoPE pair j at position pos, as (cos, sin) in fp32.  The
 // frequency theta_j = theta1^j comes from theta1 = rope_base^(-2/d_rope)
 // (formed in fp64 on the host) by repeated squaring in fp64; the angle
@@ -80,6 +79,7 @@ __device__ __forceinline__ void rope_cos_sin(double theta1, int j, int pos, floa
     sincosf((float)r, s, c);
 }
 
+// Seq length actually used: out-of-range lengths are flagged and clamped.
 __device__ __forceinline__ int clamp_len(int n, int cap, int* status) {
     if (n < 1 || n > cap) {
         flag(status, MLA_ERR_INVALID_ARG);
