@@ -1,13 +1,14 @@
 // Tensor-core GEMM for the projections around the attention core (bf16
-// operands, fp32 accumulation in TMEM): the query up-projection and its
-// absorption into latent space (first merge), the value/output projections
-// (second merge) and the cache append's down-projection, whose epilogue
-// applies RoPE and scatters rows into the paged cache.
+// operands, fp32 accumulation in TMEM): the query up-projection, whose
+// epilogue splits each head's columns into q_nope and the rotated q_pe, and
+// its absorption into latent space (first merge), the value/output
+// projections (second merge) and the cache append's down-projection, whose
+// epilogue applies RoPE and scatters rows into the paged cache.
 //
 //   C[z][m][n] = sum_k A[z][m][k] * B[z][k][n]
 //
 // 128 x 128 tiles of C, K in 64-deep slices of A (K-major) and B (K-major or
-// N-major) streamed into a 4-stage ring with TMA (128-byte swizzle);
+// N-major) streamed into a ring of stages with TMA (128-byte swizzle);
 // tcgen05.mma (M=128, N=128, K=16) accumulates in TMEM.  The kernel is
 // persistent (at most one CTA per SM, looping over work items) so that, at
 // decode batch sizes where a tile is a few k slices, the weight stream never
@@ -18,7 +19,12 @@
 // while a few stream long K ranges.  With p.splits > 1 a work item is a
 // (tile, K range) pair; its epilogue writes an fp32 partial tile to
 // p.partial[split][m][n], and splitk_reduce_kernel adds the partials and
-// applies the product's epilogue (store, or RoPE and the paged scatter).
+// applies the product's epilogue (store, RoPE and the paged scatter, or the
+// query split and rotation).
+//
+// B (or, for a skinny product, A) is the weights: the first stages' weight
+// slices are requested before the wait for the previous kernel, since no
+// kernel that may overlap this one writes them.
 //
 // Skinny products (p.swap).  The per-head query absorption and value
 // projection at decode batch sizes have M = batch rows: as the MMA's M side
