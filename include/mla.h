@@ -205,7 +205,9 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* q_pe, const
  *   1 <= q_tokens <= 64, batch * q_tokens <= 8192.
  * Each token is decoded as its own row of the split-KV plan, with the
  * sequence's block table; the rows of one sequence are adjacent in the plan,
- * so its cache rows are read from HBM about once and from L2 by the others.
+ * so workers reading the same cache tiles run at about the same time and
+ * most repeated reads hit L2 (16 sequences of 4096 tokens, 4 new tokens
+ * each: 1.6 times the cache bytes read from HBM).
  */
 int mla_decode_multi_workspace_size(const mla_config* cfg, int batch, int q_tokens,
                                     int max_blocks, size_t* bytes);
