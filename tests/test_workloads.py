@@ -134,3 +134,23 @@ def test_crossing_ranges_inputs_put_sequence_ends_inside_most_ranges():
         crossing += last > first
     assert crossing >= workers // 2
     assert 37 in lens and min(lens) >= 1
+
+
+def test_multi_token_workload_adds_a_token_axis_to_the_queries():
+    """Several new tokens per sequence: the shared-cache draws (same cache,
+    block table and weights as cached_decode with the same seed), then
+    per-token queries; deterministic in the seed."""
+    w = W.multi_token_decode(3, [4, 70, 129], 4, seed=9)
+    base = W.cached_decode(3, [4, 70, 129], seed=9, permute=True)
+    for k in ("cache", "block_table", "w_uk", "w_uv", "seq_lens"):
+        assert torch.equal(w[k], base[k])
+    assert w["q_nope"].shape == (3, 4, 128, 128) and w["q_pe"].shape == (3, 4, 128, 64)
+    assert w["kind"] == "multi" and w["q_tokens"] == 4
+    again = W.multi_token_decode(3, [4, 70, 129], 4, seed=9)
+    assert torch.equal(w["q_nope"], again["q_nope"]) and torch.equal(w["q_pe"], again["q_pe"])
+    # distinct tokens get distinct queries
+    assert not torch.equal(w["q_nope"][:, 0], w["q_nope"][:, 1])
+    v = W.oracle_view(w)
+    assert "q_tokens" not in v and v["q_nope"].shape == (3, 4, 128, 128)
+    q4 = W.WORKLOADS["v2_b16_ctx4k_q4"]
+    assert q4 is W.v2_b16_ctx4k_q4
