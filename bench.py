@@ -216,12 +216,15 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle arm
 
-def cpu_sample(w, seconds_target=12.0, max_rounds=64):
+def cpu_sample(w, seconds_target=12.0, max_rounds=64, gpu_o_lat=None):
     """Times the oracle (as it stands) on whole sequences' worth of heads.
 
     One 'round' decodes `threads` (sequence, head) pairs, one per oracle
     thread, over sequence 0's full context; rounds repeat until about
-    `seconds_target` of wall time.  Returns (tokens/s, threads, description).
+    `seconds_target` of wall time.  Returns (tokens/s, threads, description,
+    parity), parity comparing the last round's o_lat rows with the same rows
+    of `gpu_o_lat` (the GPU's o_lat for this workload, indexed like the
+    oracle's pairs) when it is given.
     """
     import oracle as O
     v = W.oracle_view(w)
@@ -232,9 +235,9 @@ def cpu_sample(w, seconds_target=12.0, max_rounds=64):
     rounds = 0
     T = w.get("q_tokens", 1)
     while True:
-        pairs = [(0, (done_heads + k) % H) for k in range(threads)]
-        _oracle_pairs(O, v, w, pairs, done_heads // H, T)
-        done_heads += threads
+        pairs = [(0, (done_heads + k) % H) for k in range(min(threads, H))]
+        ref, keys = _oracle_pairs(O, v, w, pairs, done_heads // H, T)
+        done_heads += len(pairs)
         rounds += 1
         el = time.perf_counter() - t0
         if el >= seconds_target or rounds >= max_rounds:
@@ -243,18 +246,32 @@ def cpu_sample(w, seconds_target=12.0, max_rounds=64):
     n0 = int(w["seq_lens"][0])
     desc = (f"{done_heads} (query token, head) pairs of sequence 0 (context {n0}) of "
             f"{w_name(w)}; {tokens:.3f} decode tokens in {el:.2f} s")
-    return tokens / el, threads, desc
+    parity = None
+    if gpu_o_lat is not None:
+        r = np.stack([ref[k] for k in keys]).astype(np.float64)
+        g = np.stack([gpu_o_lat[k] for k in keys]).astype(np.float64)
+        parity = {"max_rel_err": float(np.abs(g - r).max() / max(np.abs(r).max(), 1e-30)),
+                  "rows": len(keys), "tolerance": 5e-3 if w["cfg"]["dtype"] == "bf16" else 1e-5,
+                  "what": "o_lat rows of the timed workload's last oracle round against the GPU"}
+    return tokens / el, threads, desc, parity
 
 
 def _oracle_pairs(O, v, w, pairs, round_idx, T):
     """The oracle on (sequence 0, head) pairs; with several new tokens per
-    sequence, on query token round_idx % T of sequence 0."""
+    sequence, on query token round_idx % T of sequence 0.  Returns a map from
+    each pair's index into the full o_lat to the oracle's row, and the keys."""
     if w["kind"] == "cached":
-        O.reference_cached_decode(v, pairs=pairs)
-    elif w["kind"] == "multi":
-        O.reference_multi_decode(v, pairs=[(0, round_idx % T, h) for _, h in pairs])
-    else:
-        O.reference_token_decode(v, seqs=[0], pairs=[(0, h) for _, h in pairs])
+        o = O.reference_cached_decode(v, pairs=pairs)["o_lat"]
+        keys = [(0, h) for _, h in pairs]
+        return {k: o[k] for k in keys}, keys
+    if w["kind"] == "multi":
+        j = round_idx % T
+        o = O.reference_multi_decode(v, pairs=[(0, j, h) for _, h in pairs])["o_lat"]
+        keys = [(0, j, h) for _, h in pairs]
+        return {k: o[k] for k in keys}, keys
+    o = O.reference_token_decode(v, seqs=[0], pairs=[(0, h) for _, h in pairs])["o_lat"]
+    keys = [(0, h) for _, h in pairs]
+    return {k: o[k] for k in keys}, keys
 
 
 def w_name(w):
@@ -272,12 +289,12 @@ def run_reference(args):
     H = w["cfg"]["heads"]
     threads = O.num_threads()
     K = args.steps if args.steps else 5
-
     T = w.get("q_tokens", 1)
+    per = min(threads, H)     # distinct heads per step
 
     def step(i):
-        pairs = [(0, (i * threads + k) % H) for k in range(threads)]
-        _oracle_pairs(O, v, w, pairs, i * threads // H, T)
+        pairs = [(0, (i * per + k) % H) for k in range(per)]
+        _oracle_pairs(O, v, w, pairs, i * per // H, T)
 
     for i in range(args.warmup):
         step(i)
@@ -285,7 +302,7 @@ def run_reference(args):
     for i in range(K):
         step(args.warmup + i)
     el = time.perf_counter() - t0
-    tokens = K * threads / H
+    tokens = K * per / H
     val = tokens / el
     cfg = config_block(w, args.workload, 1, "n/a (host)")
     out = {
@@ -294,8 +311,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; shapes of the pages' DeepSeek-V2 figures)", "config": cfg,
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"each step: {threads} (sequence 0, head) pairs "
-                                   f"= {threads}/{H} of one decode token"},
+                         "sample": f"each step: {per} (sequence 0, head) pairs "
+                                   f"= {per}/{H} of one decode token"},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
@@ -457,9 +474,13 @@ def run_ours(args):
         "decode_path": "tcgen05" if path == 1 else "cuda-core fp32",
     }
     try:
-        cpu_val, cores, desc = cpu_sample(w)
+        s0 = steps[0]
+        o_host = s0.o_lat.float().cpu().numpy()
+        if s0.kind == "multi":
+            o_host = o_host.reshape(s0.B, s0.T, *o_host.shape[1:])
+        cpu_val, cores, desc, parity = cpu_sample(w, gpu_o_lat=o_host)
         cpu = {"value": cpu_val, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": desc}
+               "sample": desc, "parity": parity}
     except Exception as e:  # the oracle is a baseline only; report why it is missing
         cpu = {"value": None, "unit": UNIT, "cores": None, "kind": "oracle",
                "sample": f"unavailable: {e}"}

@@ -181,7 +181,9 @@ def decode(cache, block_table, seq_lens, q_nope, q_pe, w_uk, w_uv, scale, w_o=No
     wo = _f64(w_o) if w_o is not None else None
     d_model = wo.shape[1] if wo is not None else 0
     if pairs is not None:
-        plist = _i32([b * H + h for (b, h) in pairs])
+        # each (b, h) once: the C loop writes a pair's output row in place, so
+        # two threads given the same pair would interleave their sums
+        plist = _i32(sorted({b * H + h for (b, h) in pairs}))
         npairs = len(plist)
     else:
         plist, npairs = None, 0

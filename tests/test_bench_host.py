@@ -101,3 +101,19 @@ def test_committed_traffic_record_is_plausible():
     # DRAM bytes per launch are at least the algorithmic cache bytes of the
     # profiled workload (batch 16 x 4096) and not far above them
     assert 75_497_472 <= rec["dram_bytes_per_launch"] <= 1.2 * 75_497_472
+
+
+def test_cpu_sample_reports_parity_of_its_rows():
+    """The CPU-baseline leg compares the oracle's rows of its last round with
+    the same rows of the GPU's o_lat: zero error for the oracle's own full
+    result, the relative error of a perturbed one."""
+    import oracle as O
+    w = W.cached_decode(2, [40, 7], seed=2, heads=4, d_latent=8, d_rope=4, d_nope=4, d_v=4)
+    w["_name"] = "small"
+    full = O.reference_cached_decode(W.oracle_view(w))["o_lat"]
+    _, _, _, par = bench.cpu_sample(w, seconds_target=0.0, max_rounds=1, gpu_o_lat=full)
+    assert par["max_rel_err"] == 0.0 and par["rows"] >= 1
+    off = full.copy()
+    off[0] *= 1.01
+    _, _, _, par = bench.cpu_sample(w, seconds_target=0.0, max_rounds=1, gpu_o_lat=off)
+    assert abs(par["max_rel_err"] - 0.01) < 1e-9
