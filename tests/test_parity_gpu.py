@@ -92,6 +92,60 @@ def test_projection_modes_around_the_skinny_limit(batch):
         assert rel(host(res[key]), ref[key]) <= TOL["bf16"], key
 
 
+def _guarded(shape, dtype, guard=4096):
+    """A tensor of `shape` inside a larger buffer whose guard bands before and
+    after hold a canary pattern; returns (view, check) where check() is True
+    while the bands are intact."""
+    n = int(np.prod(shape))
+    buf = torch.full((guard + n + guard,), -77.0, dtype=dtype, device="cuda")
+    view = buf[guard:guard + n].view(*shape)
+    canary = torch.full((guard,), -77.0, dtype=dtype, device="cuda")
+
+    def check():
+        torch.cuda.synchronize()
+        return torch.equal(buf[:guard], canary) and torch.equal(buf[guard + n:], canary)
+    return view, check
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Canary guard bands around every output of the absorb, decode, merge,
+    value projection and multi-token calls (a stand-in for a memory checker):
+    the bands are intact afterwards and the outputs match the oracle."""
+    lens = [1, 63, 64, 65, 200, 700]
+    w = W.cached_decode(len(lens), lens, seed=70, permute=True)
+    cfg = mla.config_from(w["cfg"])
+    d = {k: w[k].cuda() for k in ("cache", "block_table", "seq_lens", "q_nope", "q_pe",
+                                  "w_uk", "w_uv")}
+    B = len(lens)
+    q_lat, c1 = _guarded((B, 128, 512), torch.bfloat16)
+    o_lat, c2 = _guarded((B, 128, 512), torch.bfloat16)
+    lse, c3 = _guarded((B, 128), torch.float32)
+    o_v, c4 = _guarded((B, 128, 128), torch.bfloat16)
+    mla.absorb_q(cfg, d["q_nope"], d["w_uk"], q_lat)
+    mla.decode(cfg, q_lat, d["q_pe"], d["cache"], d["block_table"], d["seq_lens"], o_lat, lse)
+    mla.project_out(cfg, o_lat, d["w_uv"], o_v)
+    assert c1() and c2() and c3() and c4()
+    assert mla.get_status() == mla.MLA_OK
+    ref = O.reference_cached_decode(W.oracle_view(w))
+    assert rel(host(o_lat), ref["o_lat"]) <= TOL["bf16"]
+    assert rel(host(o_v), ref["o_v"]) <= TOL["bf16"]
+
+    T = 3
+    wm = W.multi_token_decode(3, [3, 90, 200], T, seed=71)
+    dm = {k: wm[k].cuda() for k in ("cache", "block_table", "seq_lens", "q_nope", "q_pe",
+                                    "w_uk")}
+    ql = torch.empty((3 * T, 128, 512), dtype=torch.bfloat16, device="cuda")
+    mla.absorb_q(cfg, dm["q_nope"].reshape(3 * T, 128, -1), dm["w_uk"], ql)
+    om, c5 = _guarded((3, T, 128, 512), torch.bfloat16)
+    lm, c6 = _guarded((3, T, 128), torch.float32)
+    mla.decode_multi(cfg, ql.view(3, T, 128, 512), dm["q_pe"], dm["cache"], dm["block_table"],
+                     dm["seq_lens"], om, lm)
+    assert c5() and c6()
+    assert mla.get_status() == mla.MLA_OK
+    refm = O.reference_multi_decode(W.oracle_view(wm))
+    assert rel(host(om), refm["o_lat"]) <= TOL["bf16"]
+
+
 def test_seq_len_one_returns_the_cached_latent():
     w = W.cached_decode(3, [1, 1, 1], seed=5, permute=True)
     step = run_step(w)
