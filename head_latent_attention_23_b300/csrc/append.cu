@@ -1,5 +1,10 @@
 // Cache append: down-projection of new tokens to [latent | rotary key] rows,
-// RoPE on the rotary part, scatter into the paged cache.
+// RoPE on the rotary part, scatter into the paged cache (CUDA cores; the bf16
+// append runs in the tensor-core GEMM's epilogue).  Also the small kernels
+// around the projections: the query split and rotation for fp32
+// configurations, the per-(sequence, pair) rotation table of the fused bf16
+// query epilogue, the positions of a layer step and the per-token rows of a
+// multi-token decode.
 //
 // "Multi-Head Latent Attention (MLA)", "The construction": the cached object
 // is L = X W_L, one d_latent row per token for all heads; "The RoPE problem":
