@@ -386,6 +386,42 @@ def test_page_permutation_is_invisible():
     assert np.array_equal(a["o_lat"], c["o_lat"]) and np.array_equal(a["o_v"], c["o_v"])
 
 
+def test_multi_token_first_token_sees_only_its_prefix():
+    """Several new tokens: the first of T tokens of a sequence of n attends to
+    n - T + 1 rows, so changing any of the T - 1 newest rows leaves it
+    unchanged and changes the last token (the causal mask of section 03); a
+    token's result equals a one-token decode of the same query over the
+    sequence cut at its position, brute force by single-element loops."""
+    p = _cached_problem(21, n=8)
+    T, lens = 3, [8, 6]
+    r = _rng(22)
+    qn = r.standard_normal((p["B"], T, p["H"], p["q_nope"].shape[2]))
+    qp = r.standard_normal((p["B"], T, p["H"], p["d_r"]))
+    a = O.decode_multi(p["cache"], p["bt"], lens, qn, qp, p["w_uk"], p["w_uv"], p["scale"])
+    q = dict(p)
+    q["cache"] = p["cache"].copy()
+    flat = q["cache"].reshape(-1, p["d_l"] + p["d_r"])
+    for b, n in enumerate(lens):
+        for i in range(n - T + 1, n):
+            flat[O.slot(p["bt"], p["bs"], p["cache"].shape[0], b, i)] += 0.5
+    c = O.decode_multi(q["cache"], p["bt"], lens, qn, qp, p["w_uk"], p["w_uv"], p["scale"])
+    assert np.array_equal(a["o_lat"][:, 0], c["o_lat"][:, 0])
+    assert not np.allclose(a["o_lat"][:, T - 1], c["o_lat"][:, T - 1])
+    # token j of sequence b, head h, by hand: scores over rows 0..n-T+j
+    for b, n in enumerate(lens):
+        for j in range(T):
+            m = n - T + 1 + j
+            for h in range(p["H"]):
+                qlat = p["w_uk"][h] @ qn[b, j, h]                 # [d_l]
+                s = np.array([p["scale"] * (qlat @ _row(p, b, i)[:p["d_l"]] +
+                                            qp[b, j, h] @ _row(p, b, i)[p["d_l"]:])
+                              for i in range(m)])
+                w = np.exp(s - s.max())
+                w /= w.sum()
+                o = sum(w[i] * _row(p, b, i)[:p["d_l"]] for i in range(m))
+                assert _rel(a["o_lat"][b, j, h], o) < 1e-12
+
+
 def test_index_map_golden():
     with open(os.path.join(GOLDEN, "paged_index_map.json")) as f:
         g = json.load(f)
