@@ -112,3 +112,19 @@ def test_multi_token_decode_validates_on_the_host(L):
     # a valid shape with null tensors is refused before any CUDA call
     assert L.mla_decode_multi(cp, None, None, None, 1, None, 8, None, 4, 2, None, None, None, 0,
                               None) == mla.MLA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_header_is_plain_c_and_cpp(lang, std, tmp_path):
+    """include/mla.h is a C ABI: it compiles on its own as C99 and as C++11,
+    with warnings as errors, and needs no CUDA or torch header."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use.c" if lang == "c" else "use.cpp")
+    src.write_text('#include "mla.h"\nint probe(void) { return mla_version() > 0 ? MLA_OK : MLA_ERR_CUDA; }\n')
+    r = subprocess.run([cc, "-fsyntax-only", "-Wall", "-Wextra", "-Werror", std, "-I",
+                        os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
